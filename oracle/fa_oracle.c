@@ -1,0 +1,234 @@
+/*
+ * Test infrastructure, not product code: a plain, slow fp64 CPU oracle for
+ * exact scaled-dot-product attention. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load or call it; the CUDA library never
+ * does, and this file shares no code with it.
+ *
+ * It computes the definition of attention written out, not a tiled
+ * algorithm. The pages state that the IO-aware method returns exactly
+ * softmax(Q K^T) V "with no approximation" ("FlashAttention does more
+ * arithmetic to move less data", section "FlashAttention never writes the
+ * full score table to HBM"; "FlashAttention and GPU Memory", chapter 01 and
+ * chapter 12), so the definition is the oracle.
+ *
+ * Layout: q, k, v, dO, o, dq, dk, dv are [BH][N][d] row-major doubles; lse
+ * and D are [BH][N]. Row i attends to A(i) = {0..N-1}, or {0..i} when causal
+ * (the pages name a fused "mask" without defining it; the causal reading
+ * j <= i is the plainest one and makes row 0 attend to key 0 only).
+ *
+ * Forward, per head and row i (chapter 08 defines the row max m and the sum
+ * of exponentials l that the tiled method carries; here they are taken over
+ * the whole row at once):
+ *   s_ij = scale * q_i . k_j          (j in A(i))
+ *   M_i  = max_j s_ij
+ *   l_i  = sum_j exp(s_ij - M_i)
+ *   P_ij = exp(s_ij - M_i) / l_i
+ *   o_i  = sum_j P_ij v_j
+ *   lse_i = M_i + ln l_i              (the natural-log logsumexp of the row)
+ *
+ * Backward, by the chain rule on the same definition (the pages only say that
+ * S and P are rebuilt from Q, K, V and the saved row statistics, chapter 09):
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_{j in A(i)} P_ij dP_ij   (summed explicitly, not as dO_i . o_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dq_i  = scale * sum_j dS_ij k_j
+ *   dk_j  = scale * sum_i dS_ij q_i
+ *   dv_j  = sum_i P_ij dO_i
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double dot(const double* a, const double* b, int d) {
+  double acc = 0.0;
+  for (int t = 0; t < d; ++t) acc += a[t] * b[t];
+  return acc;
+}
+
+static int row_len(int i, int N, int causal) { return causal ? i + 1 : N; }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+}
+
+/* Scores, max and sum of exponentials for row i of one head. s has room for N. */
+static void score_row(const double* qi, const double* k, int n, int d, double scale, double* s, double* M_out,
+                      double* l_out) {
+  double M = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    s[j] = scale * dot(qi, k + (size_t)j * d, d);
+    if (s[j] > M) M = s[j];
+  }
+  double l = 0.0;
+  for (int j = 0; j < n; ++j) l += exp(s[j] - M);
+  *M_out = M;
+  *l_out = l;
+}
+
+/*
+ * Forward pass. rows == NULL computes every row; otherwise only the nrows
+ * listed rows of every head are written (o rows and lse entries elsewhere are
+ * left untouched). Returns 0, or -1 on a bad argument or allocation failure.
+ */
+int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int N, int d,
+               double scale, int causal, const int* rows, int nrows, int nthreads) {
+  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
+  if (!rows) nrows = N;
+  for (int r = 0; rows && r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return -1;
+  set_threads(nthreads);
+  int failed = 0;
+  const long long total = (long long)BH * nrows;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long long w = 0; w < total; ++w) {
+      if (!s) continue;
+      const int h = (int)(w / nrows);
+      const int i = rows ? rows[w % nrows] : (int)(w % nrows);
+      const size_t hb = (size_t)h * N * d;
+      const double* qi = q + hb + (size_t)i * d;
+      const int n = row_len(i, N, causal);
+      double M, l;
+      score_row(qi, k + hb, n, d, scale, s, &M, &l);
+      double* oi = o + hb + (size_t)i * d;
+      for (int t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int j = 0; j < n; ++j) {
+        const double p = exp(s[j] - M) / l;
+        const double* vj = v + hb + (size_t)j * d;
+        for (int t = 0; t < d; ++t) oi[t] += p * vj[t];
+      }
+      lse[(size_t)h * N + i] = M + log(l);
+    }
+    free(s);
+  }
+  return failed ? -1 : 0;
+}
+
+/*
+ * Backward pass. Every row's lse and D are computed (both are needed by every
+ * key's gradient). dq is written for the listed query rows (qrows == NULL:
+ * all rows), dk and dv for the listed keys (keys == NULL: all keys). D, if
+ * non-NULL, receives D_i for every row. Returns 0, or -1 on error.
+ */
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
+               double* dv, double* D, int BH, int N, int d, double scale, int causal, const int* qrows, int nq,
+               const int* keys, int nk, int nthreads) {
+  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !dO || !dq || !dk || !dv) return -1;
+  if (!qrows) nq = N;
+  if (!keys) nk = N;
+  for (int r = 0; qrows && r < nq; ++r)
+    if (qrows[r] < 0 || qrows[r] >= N) return -1;
+  for (int r = 0; keys && r < nk; ++r)
+    if (keys[r] < 0 || keys[r] >= N) return -1;
+  set_threads(nthreads);
+  double* lse_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  double* D_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  char* want_q = (char*)calloc((size_t)N, 1);
+  if (!lse_all || !D_all || !want_q) {
+    free(lse_all);
+    free(D_all);
+    free(want_q);
+    return -1;
+  }
+  for (int r = 0; r < nq; ++r) want_q[qrows ? qrows[r] : r] = 1;
+  int failed = 0;
+
+  /* Pass 1, one query row at a time: P, dP, D and dS of the row; dq. */
+  const long long total_rows = (long long)BH * N;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s || !dp) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long long w = 0; w < total_rows; ++w) {
+      if (!s || !dp) continue;
+      const int h = (int)(w / N), i = (int)(w % N);
+      const size_t hb = (size_t)h * N * d;
+      const double* qi = q + hb + (size_t)i * d;
+      const double* dOi = dO + hb + (size_t)i * d;
+      const int n = row_len(i, N, causal);
+      double M, l;
+      score_row(qi, k + hb, n, d, scale, s, &M, &l);
+      double Di = 0.0;
+      for (int j = 0; j < n; ++j) {
+        s[j] = exp(s[j] - M) / l; /* s now holds P_ij */
+        dp[j] = dot(dOi, v + hb + (size_t)j * d, d);
+        Di += s[j] * dp[j];
+      }
+      lse_all[w] = M + log(l);
+      D_all[w] = Di;
+      if (want_q[i]) {
+        double* dqi = dq + hb + (size_t)i * d;
+        for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+        for (int j = 0; j < n; ++j) {
+          const double ds = s[j] * (dp[j] - Di);
+          const double* kj = k + hb + (size_t)j * d;
+          for (int t = 0; t < d; ++t) dqi[t] += scale * ds * kj[t];
+        }
+      }
+    }
+    free(s);
+    free(dp);
+  }
+
+  /* Pass 2, one key at a time: dk and dv sum over the rows that see key j. */
+  const long long total_keys = (long long)BH * nk;
+  if (!failed) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long w = 0; w < total_keys; ++w) {
+      const int h = (int)(w / nk);
+      const int j = keys ? keys[w % nk] : (int)(w % nk);
+      const size_t hb = (size_t)h * N * d;
+      const double* kj = k + hb + (size_t)j * d;
+      const double* vj = v + hb + (size_t)j * d;
+      double* dkj = dk + hb + (size_t)j * d;
+      double* dvj = dv + hb + (size_t)j * d;
+      for (int t = 0; t < d; ++t) {
+        dkj[t] = 0.0;
+        dvj[t] = 0.0;
+      }
+      for (int i = causal ? j : 0; i < N; ++i) {
+        const double* qi = q + hb + (size_t)i * d;
+        const double* dOi = dO + hb + (size_t)i * d;
+        const double p = exp(scale * dot(qi, kj, d) - lse_all[(size_t)h * N + i]);
+        const double ds = p * (dot(dOi, vj, d) - D_all[(size_t)h * N + i]);
+        for (int t = 0; t < d; ++t) {
+          dkj[t] += scale * ds * qi[t];
+          dvj[t] += p * dOi[t];
+        }
+      }
+    }
+  }
+  if (D && !failed) memcpy(D, D_all, sizeof(double) * (size_t)BH * N);
+  free(lse_all);
+  free(D_all);
+  free(want_q);
+  return failed ? -1 : 0;
+}
+
+/* Number of threads an OpenMP parallel region would use (1 without OpenMP). */
+int oracle_max_threads(int nthreads) {
+  set_threads(nthreads);
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

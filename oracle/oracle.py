@@ -1,0 +1,210 @@
+"""Test infrastructure, not product code: the fp64 CPU oracle for exact attention.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this module. The CUDA library and its Python binding never
+touch it, and it imports nothing from them.
+
+Three independent views of the same definition live here:
+
+* ``fwd`` / ``bwd`` call the streaming C implementation in ``fa_oracle.c``
+  (the definition, row by row, fp64, OpenMP over rows and keys);
+* ``materialised_fwd`` / ``materialised_bwd`` build the full N x N score
+  matrix S and probability matrix P with numpy, in the order the pages call
+  "the standard way" ("FlashAttention and GPU Memory", chapter 04: S = QK^T,
+  then P = softmax(S), then O = PV), for tiny inputs only;
+* ``online_softmax`` carries the running maximum m and running sum l block by
+  block, with the update rule of chapter 08 of the same page
+  (m_new = max(m, m~), l_new = e^(m - m_new) l + e^(m~ - m_new) l~), so that the
+  page's claim that the blocked result equals the whole-row softmax can be
+  checked.
+
+Arrays are numpy float64 of shape [BH, N, d] (lse and D: [BH, N]).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle with gcc (-O2, OpenMP, no fast-math) into a shared library."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the C oracle and declare its signatures."""
+    global _lib
+    with _lock:
+        if path is None and _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(path or build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        c_int, c_double = ctypes.c_int, ctypes.c_double
+        lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, ip, c_int, c_int]
+        lib.oracle_fwd.restype = c_int
+        lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int,
+                                   ip, c_int, ip, c_int, c_int]
+        lib.oracle_bwd.restype = c_int
+        lib.oracle_max_threads.argtypes = [c_int]
+        lib.oracle_max_threads.restype = c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    """Contiguous float64 numpy copy of a numpy array or a (CPU) torch tensor."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _as3(a: np.ndarray) -> np.ndarray:
+    return a.reshape(-1, a.shape[-2], a.shape[-1])
+
+
+def _dptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _iptr(idx):
+    if idx is None:
+        return None, 0
+    arr = np.ascontiguousarray(idx, dtype=np.int32)
+    return arr, len(arr)
+
+
+def max_threads(nthreads: int = 0) -> int:
+    return int(load().oracle_max_threads(nthreads))
+
+
+def fwd(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None):
+    """O and lse of softmax(scale * q k^T [causal]) v, fp64.
+
+    ``rows`` (optional) restricts the computation to those query rows of every
+    head; the other rows of the returned arrays are NaN.
+    """
+    lib = lib or load()
+    q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
+    BH, N, d = q3.shape
+    o = np.full_like(q3, np.nan)
+    lse = np.full((BH, N), np.nan)
+    ridx, nr = _iptr(rows)
+    rc = lib.oracle_fwd(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(o), _dptr(lse), BH, N, d, float(scale), int(causal),
+                        None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nr, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_fwd failed")
+    return o, lse
+
+
+def bwd(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads: int = 0, lib=None):
+    """dq, dk, dv and D (D_i = sum_j P_ij dP_ij) of L = sum(dO * O), fp64.
+
+    ``qrows`` / ``keys`` (optional) restrict which dq rows / dk and dv rows
+    are computed; the rest are NaN. D is always complete.
+    """
+    lib = lib or load()
+    q3, k3, v3, dO3 = (_as3(_f64(x)) for x in (q, k, v, dO))
+    BH, N, d = q3.shape
+    dq = np.full_like(q3, np.nan)
+    dk = np.full_like(q3, np.nan)
+    dv = np.full_like(q3, np.nan)
+    D = np.full((BH, N), np.nan)
+    qi, nq = _iptr(qrows)
+    ki, nk = _iptr(keys)
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = lib.oracle_bwd(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(dO3), _dptr(dq), _dptr(dk), _dptr(dv), _dptr(D),
+                        BH, N, d, float(scale), int(causal),
+                        None if qi is None else qi.ctypes.data_as(ip), nq,
+                        None if ki is None else ki.ctypes.data_as(ip), nk, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_bwd failed")
+    return dq, dk, dv, D
+
+
+# --------------------------------------------------------------------------
+# The standard, materialised computation (tiny inputs only).
+# --------------------------------------------------------------------------
+def _mask(N: int, causal: bool) -> np.ndarray:
+    """True where key j is visible to query i: every j, or j <= i when causal."""
+    allowed = np.ones((N, N), dtype=bool)
+    if causal:
+        allowed = np.tril(allowed)
+    return allowed
+
+
+def materialised_fwd(q, k, v, scale: float, causal: bool):
+    """S, then P = softmax(S), then O = P V, each a full matrix per head."""
+    q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
+    N = q3.shape[1]
+    S = scale * np.matmul(q3, np.swapaxes(k3, 1, 2))
+    S = np.where(_mask(N, causal)[None], S, -np.inf)
+    M = S.max(axis=2, keepdims=True)
+    E = np.exp(S - M)
+    ell = E.sum(axis=2, keepdims=True)
+    P = E / ell
+    O = np.matmul(P, v3)
+    lse = (M + np.log(ell))[..., 0]
+    return O, lse, S, P
+
+
+def materialised_bwd(q, k, v, dO, scale: float, causal: bool):
+    """Gradients from the full P and dP matrices (tiny inputs only)."""
+    q3, k3, v3, dO3 = (_as3(_f64(x)) for x in (q, k, v, dO))
+    _, _, _, P = materialised_fwd(q3, k3, v3, scale, causal)
+    dP = np.matmul(dO3, np.swapaxes(v3, 1, 2))
+    D = (P * dP).sum(axis=2, keepdims=True)
+    dS = P * (dP - D)
+    dq = scale * np.matmul(dS, k3)
+    dk = scale * np.matmul(np.swapaxes(dS, 1, 2), q3)
+    dv = np.matmul(np.swapaxes(P, 1, 2), dO3)
+    return dq, dk, dv, D[..., 0]
+
+
+# --------------------------------------------------------------------------
+# Online softmax over one row, block by block.
+# --------------------------------------------------------------------------
+def online_softmax(scores, values, block: int):
+    """Running max m and running sum l over a row of scores, ``block`` at a time.
+
+    Each block brings its own max m~ and sum l~ = sum exp(s - m~) and its own
+    partial output o~ = sum exp(s - m~) v; the running state moves to the new
+    reference max with the factor e^(m - m_new). Returns (m, l, o / l) after
+    the last block.
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    vals = np.asarray(values, dtype=np.float64)
+    m, ell = -np.inf, 0.0
+    o = np.zeros(vals.shape[1:], dtype=np.float64)
+    for start in range(0, len(s), block):
+        sb, vb = s[start:start + block], vals[start:start + block]
+        m_blk = sb.max()
+        e = np.exp(sb - m_blk)
+        l_blk = e.sum()
+        o_blk = e @ vb
+        m_new = max(m, m_blk)
+        a_old = np.exp(m - m_new) if np.isfinite(m) else 0.0
+        a_blk = np.exp(m_blk - m_new)
+        ell = a_old * ell + a_blk * l_blk
+        o = a_old * o + a_blk * o_blk
+        m = m_new
+    return m, ell, o / ell

@@ -1,0 +1,237 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes an oracle library handle (``None`` = the real
+one) and raises AssertionError when the oracle disagrees with a closed form,
+an invariant, a library routine (torch's fp64 CPU scaled_dot_product_attention
+and autograd) or central finite differences. The same functions are run
+against deliberately broken copies of the oracle to show that each plausible
+mistake is caught.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from oracle import oracle as orc
+
+
+def _rand(rng, *shape, scale=1.0):
+    return rng.standard_normal(shape) * scale
+
+
+def _qkv(seed, BH, N, d, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return (_rand(rng, BH, N, d, scale=scale), _rand(rng, BH, N, d, scale=scale), _rand(rng, BH, N, d),
+            _rand(rng, BH, N, d))
+
+
+def pin_zero_q_noncausal(lib=None):
+    """Q = 0: every score is 0, P is uniform, each output row is the mean of V; lse = ln N."""
+    rng = np.random.default_rng(1)
+    BH, N, d = 2, 37, 8
+    q = np.zeros((BH, N, d))
+    k, v = _rand(rng, BH, N, d), _rand(rng, BH, N, d)
+    o, lse = orc.fwd(q, k, v, 0.3, False, lib=lib)
+    assert np.allclose(o, v.mean(axis=1, keepdims=True), rtol=0, atol=1e-13)
+    assert np.allclose(lse, math.log(N), rtol=0, atol=1e-13)
+
+
+def pin_zero_q_causal(lib=None):
+    """Q = 0, causal: row i is the mean of v_0..v_i, row 0 is exactly v_0; lse_i = ln(i + 1)."""
+    rng = np.random.default_rng(2)
+    BH, N, d = 2, 29, 8
+    q = np.zeros((BH, N, d))
+    k, v = _rand(rng, BH, N, d), _rand(rng, BH, N, d)
+    o, lse = orc.fwd(q, k, v, 0.7, True, lib=lib)
+    prefix = np.cumsum(v, axis=1) / np.arange(1, N + 1)[None, :, None]
+    assert np.allclose(o, prefix, rtol=0, atol=1e-13)
+    assert np.array_equal(o[:, 0], v[:, 0])
+    assert np.allclose(lse, np.log(np.arange(1, N + 1))[None], rtol=0, atol=1e-13)
+
+
+def pin_single_key(lib=None):
+    """N = 1: O = V, lse = scale q.k, dq = dk = 0, dv = dO."""
+    rng = np.random.default_rng(3)
+    BH, N, d = 3, 1, 5
+    q, k, v, dO = (_rand(rng, BH, N, d) for _ in range(4))
+    for causal in (False, True):
+        o, lse = orc.fwd(q, k, v, 0.4, causal, lib=lib)
+        assert np.allclose(o, v, rtol=0, atol=1e-15)
+        assert np.allclose(lse, 0.4 * np.einsum("bnd,bnd->bn", q, k), rtol=0, atol=1e-14)
+        dq, dk, dv, _ = orc.bwd(q, k, v, dO, 0.4, causal, lib=lib)
+        assert np.allclose(dq, 0, atol=1e-15) and np.allclose(dk, 0, atol=1e-15)
+        assert np.allclose(dv, dO, rtol=0, atol=1e-15)
+
+
+def pin_two_keys(lib=None):
+    """N = 2 without mask: the softmax of two scores is a logistic function of their difference."""
+    rng = np.random.default_rng(4)
+    d, scale = 6, 0.8
+    q, k, v = _rand(rng, 1, 2, d), _rand(rng, 1, 2, d), _rand(rng, 1, 2, d)
+    o, lse = orc.fwd(q, k, v, scale, False, lib=lib)
+    for i in range(2):
+        s0 = scale * float(q[0, i] @ k[0, 0])
+        s1 = scale * float(q[0, i] @ k[0, 1])
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        assert np.allclose(o[0, i], w0 * v[0, 0] + (1.0 - w0) * v[0, 1], rtol=0, atol=1e-14)
+        assert abs(lse[0, i] - np.logaddexp(s0, s1)) < 1e-14
+
+
+def _torch_ref(q, k, v, dO, scale, causal):
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    o.backward(torch.tensor(dO, dtype=torch.float64))
+    return o.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def pin_torch_sdpa(lib=None):
+    """O and gradients against torch's fp64 CPU scaled_dot_product_attention and autograd."""
+    for seed, (BH, N, d) in enumerate([(2, 1, 4), (2, 7, 16), (3, 33, 8), (1, 64, 32)]):
+        q, k, v, dO = _qkv(10 + seed, BH, N, d)
+        for causal in (False, True):
+            scale = 1.0 / math.sqrt(d) * (1.5 if seed % 2 else 1.0)
+            o_ref, dq_ref, dk_ref, dv_ref = _torch_ref(q, k, v, dO, scale, causal)
+            o, lse = orc.fwd(q, k, v, scale, causal, lib=lib)
+            assert np.allclose(o, o_ref, rtol=0, atol=1e-12), (N, d, causal)
+            dq, dk, dv, _ = orc.bwd(q, k, v, dO, scale, causal, lib=lib)
+            for g, r in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+                assert np.allclose(g, r, rtol=0, atol=1e-11), (N, d, causal)
+
+
+def pin_lse_logsumexp(lib=None):
+    """lse is torch.logsumexp of the scaled, masked score row; and max <= lse <= max + ln|A(i)|."""
+    q, k, v, _ = _qkv(20, 2, 19, 8)
+    scale = 0.6
+    for causal in (False, True):
+        _, lse = orc.fwd(q, k, v, scale, causal, lib=lib)
+        S = scale * torch.einsum("bid,bjd->bij", torch.tensor(q), torch.tensor(k))
+        if causal:
+            S = S.masked_fill(torch.ones(19, 19, dtype=torch.bool).triu(1), float("-inf"))
+        ref = torch.logsumexp(S, dim=-1).numpy()
+        assert np.allclose(lse, ref, rtol=0, atol=1e-13)
+        smax = S.max(dim=-1).values.numpy()
+        cnt = np.arange(1, 20) if causal else np.full(19, 19)
+        assert np.all(lse >= smax - 1e-13) and np.all(lse <= smax + np.log(cnt)[None] + 1e-13)
+
+
+def pin_finite_differences(lib=None):
+    """Gradients of L = sum(dO * O) against central differences (h = 1e-6)."""
+    q, k, v, dO = _qkv(30, 1, 6, 3)
+    scale, h = 0.9, 1e-6
+    for causal in (False, True):
+        dq, dk, dv, _ = orc.bwd(q, k, v, dO, scale, causal, lib=lib)
+
+        def loss(qq, kk, vv):
+            o, _ = orc.fwd(qq, kk, vv, scale, causal, lib=lib)
+            return float((o * dO).sum())
+
+        for which, grad in ((0, dq), (1, dk), (2, dv)):
+            for idx in [(0, 0, 0), (0, 2, 1), (0, 5, 2), (0, 3, 0)]:
+                args = [q.copy(), k.copy(), v.copy()]
+                args[which][idx] += h
+                lp = loss(*args)
+                args[which][idx] -= 2 * h
+                lm = loss(*args)
+                fd = (lp - lm) / (2 * h)
+                assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, causal, fd, grad[idx])
+
+
+def pin_key_shift(lib=None):
+    """K -> K + 1 u^T adds scale q_i.u to every score of row i: O, dq, dk, dv unchanged, lse shifted."""
+    q, k, v, dO = _qkv(40, 2, 23, 8)
+    u = np.random.default_rng(41).standard_normal(8)
+    scale = 0.5
+    for causal in (False, True):
+        o0, l0 = orc.fwd(q, k, v, scale, causal, lib=lib)
+        o1, l1 = orc.fwd(q, k + u, v, scale, causal, lib=lib)
+        assert np.allclose(o0, o1, rtol=0, atol=1e-12)
+        assert np.allclose(l1 - l0, scale * np.einsum("bid,d->bi", q, u), rtol=0, atol=1e-12)
+        g0 = orc.bwd(q, k, v, dO, scale, causal, lib=lib)
+        g1 = orc.bwd(q, k + u, v, dO, scale, causal, lib=lib)
+        for a, b in zip(g0[:3], g1[:3]):
+            assert np.allclose(a, b, rtol=0, atol=1e-11)
+
+
+def pin_value_shift_and_linearity(lib=None):
+    """Rows of P sum to 1: V -> V + 1 w^T adds w to every output row; O is linear in V."""
+    q, k, v, _ = _qkv(50, 2, 17, 8)
+    w = np.random.default_rng(51).standard_normal(8)
+    v2 = np.random.default_rng(52).standard_normal(v.shape)
+    for causal in (False, True):
+        o0, l0 = orc.fwd(q, k, v, 0.7, causal, lib=lib)
+        o1, l1 = orc.fwd(q, k, v + w, 0.7, causal, lib=lib)
+        assert np.allclose(o1, o0 + w, rtol=0, atol=1e-12) and np.allclose(l0, l1, rtol=0, atol=0)
+        o2, _ = orc.fwd(q, k, v2, 0.7, causal, lib=lib)
+        o3, _ = orc.fwd(q, k, 2.0 * v - 3.0 * v2, 0.7, causal, lib=lib)
+        assert np.allclose(o3, 2.0 * o0 - 3.0 * o2, rtol=0, atol=1e-11)
+
+
+def pin_permutation(lib=None):
+    """Without a mask, permuting K and V rows together leaves O, lse, dq unchanged and permutes dk, dv."""
+    q, k, v, dO = _qkv(60, 2, 13, 4)
+    perm = np.random.default_rng(61).permutation(13)
+    o0, l0 = orc.fwd(q, k, v, 0.8, False, lib=lib)
+    o1, l1 = orc.fwd(q, k[:, perm], v[:, perm], 0.8, False, lib=lib)
+    assert np.allclose(o0, o1, rtol=0, atol=1e-13) and np.allclose(l0, l1, rtol=0, atol=1e-13)
+    dq0, dk0, dv0, _ = orc.bwd(q, k, v, dO, 0.8, False, lib=lib)
+    dq1, dk1, dv1, _ = orc.bwd(q, k[:, perm], v[:, perm], dO, 0.8, False, lib=lib)
+    assert np.allclose(dq0, dq1, rtol=0, atol=1e-13)
+    assert np.allclose(dk0[:, perm], dk1, rtol=0, atol=1e-13)
+    assert np.allclose(dv0[:, perm], dv1, rtol=0, atol=1e-13)
+
+
+def pin_gradient_identities(lib=None):
+    """sum_j dS_ij = 0 gives sum_j dk_j = 0; D_i = sum_j P_ij dP_ij equals dO_i . o_i."""
+    q, k, v, dO = _qkv(70, 3, 21, 8)
+    for causal in (False, True):
+        o, _ = orc.fwd(q, k, v, 0.6, causal, lib=lib)
+        dq, dk, dv, D = orc.bwd(q, k, v, dO, 0.6, causal, lib=lib)
+        assert np.allclose(dk.sum(axis=1), 0, atol=1e-12)
+        assert np.allclose(D, np.einsum("bid,bid->bi", dO, o), rtol=0, atol=1e-12)
+        # sum over keys of dv equals sum over rows of dO (columns of P^T sum the rows' unit mass)
+        assert np.allclose(dv.sum(axis=1), dO.sum(axis=1), rtol=0, atol=1e-11)
+
+
+def pin_zero_q_dv(lib=None):
+    """Q = 0, no mask: P = 1/N everywhere, so dv_j = (1/N) sum_i dO_i and dk = 0."""
+    rng = np.random.default_rng(80)
+    BH, N, d = 2, 11, 5
+    q = np.zeros((BH, N, d))
+    k, v, dO = (_rand(rng, BH, N, d) for _ in range(3))
+    _, dk, dv, _ = orc.bwd(q, k, v, dO, 0.9, False, lib=lib)
+    assert np.allclose(dv, dO.mean(axis=1, keepdims=True), rtol=0, atol=1e-14)
+    assert np.allclose(dk, 0, atol=1e-14)
+
+
+def pin_sampling(lib=None):
+    """Row- and key-restricted calls return exactly the corresponding rows of the full call."""
+    q, k, v, dO = _qkv(90, 2, 40, 8)
+    rows = [0, 5, 39, 17]
+    for causal in (False, True):
+        o, lse = orc.fwd(q, k, v, 0.5, causal, lib=lib)
+        os_, ls_ = orc.fwd(q, k, v, 0.5, causal, rows=rows, lib=lib)
+        assert np.array_equal(o[:, rows], os_[:, rows]) and np.array_equal(lse[:, rows], ls_[:, rows])
+        dq, dk, dv, D = orc.bwd(q, k, v, dO, 0.5, causal, lib=lib)
+        dq2, dk2, dv2, D2 = orc.bwd(q, k, v, dO, 0.5, causal, qrows=rows, keys=[1, 39, 2], lib=lib)
+        assert np.array_equal(dq[:, rows], dq2[:, rows]) and np.array_equal(D, D2)
+        assert np.array_equal(dk[:, [1, 39, 2]], dk2[:, [1, 39, 2]])
+        assert np.array_equal(dv[:, [1, 39, 2]], dv2[:, [1, 39, 2]])
+
+
+ALL_PINS = [
+    pin_zero_q_noncausal,
+    pin_zero_q_causal,
+    pin_single_key,
+    pin_two_keys,
+    pin_torch_sdpa,
+    pin_lse_logsumexp,
+    pin_finite_differences,
+    pin_key_shift,
+    pin_value_shift_and_linearity,
+    pin_permutation,
+    pin_gradient_identities,
+    pin_zero_q_dv,
+    pin_sampling,
+]

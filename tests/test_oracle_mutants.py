@@ -1,0 +1,45 @@
+"""Plants plausible mistakes in a copy of the C oracle (on the CPU) and checks
+that the pins catch every one: a pin that a wrong oracle also passes pins
+nothing."""
+import os
+import shutil
+
+import pytest
+
+from oracle import oracle as orc
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(orc.__file__), "fa_oracle.c")
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("dropped_scale", "s[j] = scale * dot(qi, k + (size_t)j * d, d);", "s[j] = dot(qi, k + (size_t)j * d, d);"),
+    ("causal_excludes_diagonal", "return causal ? i + 1 : N;", "return causal ? (i > 0 ? i : 1) : N;"),
+    ("lse_without_log_sum", "lse[(size_t)h * N + i] = M + log(l);", "lse[(size_t)h * N + i] = M;"),
+    ("output_reads_k_not_v", "const double* vj = v + hb + (size_t)j * d;\n        for (int t = 0; t < d; ++t) oi[t]",
+     "const double* vj = k + hb + (size_t)j * d;\n        for (int t = 0; t < d; ++t) oi[t]"),
+    ("D_wrong_sign", "Di += s[j] * dp[j];", "Di -= s[j] * dp[j];"),
+    ("dq_dropped_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
+    ("dk_transposed_operand", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
+    ("dv_uses_dS", "dvj[t] += p * dOi[t];", "dvj[t] += ds * dOi[t];"),
+    ("bwd_causal_skips_diagonal", "for (int i = causal ? j : 0; i < N; ++i)", "for (int i = causal ? j + 1 : 0; i < N; ++i)"),
+    ("bwd_mask_reversed", "for (int i = causal ? j : 0; i < N; ++i)", "for (int i = 0; i < (causal ? j + 1 : N); ++i)"),
+    ("dp_uses_o_index", "dp[j] = dot(dOi, v + hb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + hb + (size_t)i * d, d);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not unique"
+    src = tmp_path / "fa_oracle_mutant.c"
+    src.write_text(text.replace(old, new))
+    so = orc.build(force=True, src=str(src), out=str(tmp_path / "libmutant.so"))
+    lib = orc.load(so)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, RuntimeError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught mutant {name}"
