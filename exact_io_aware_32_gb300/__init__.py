@@ -1,0 +1,9 @@
+"""Exact, IO-aware scaled-dot-product attention for NVIDIA GB300 (sm_103a).
+
+The kernels sit behind the C ABI of ``include/fa.h`` (``libfa.so``); this
+package holds the thin ctypes binding (``fa``), the build script, the seeded
+input generators and the flop/byte model the benchmark reports against.
+"""
+from .fa import (  # noqa: F401
+    FA_OK, FAError, backward, fa_bwd, fa_bwd_workspace_bytes, fa_device_status, fa_fwd, fa_status_string, forward,
+)

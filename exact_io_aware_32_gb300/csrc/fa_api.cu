@@ -1,0 +1,203 @@
+// C ABI of the attention library (declared in include/fa.h): argument
+// checks, TMA tensor-map encoding, and kernel launches. Nothing here
+// allocates device memory; the only device state the library owns is one
+// error word per device, a file-scope __device__ variable.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+__device__ unsigned int g_fa_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  bool supported = false;
+  unsigned int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int fail_launch() { return FA_ERR_LAUNCH; }
+
+// Per-device facts, looked up once per device with that device current.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail_launch();
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail_launch();
+    di.supported = (major == 10 && minor == 3);  // the kernels are built for sm_103a only
+    di.num_sms = sms;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_device_status) != cudaSuccess) return fail_launch();
+    di.status = static_cast<unsigned int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return fail_launch();
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    di.ready = true;
+  }
+  if (!di.supported) return FA_ERR_UNSUPPORTED;
+  *out = &di;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const long long total = (long long)B * H * N * d;
+  if ((long long)B * H > INT32_MAX || total >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Tensor map over a contiguous [BH][N][d] tensor, boxes of box_x columns by
+// box_rows rows of one head, 128-byte swizzle (box_x * elem == 128 bytes).
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem, int BH, int N, int d,
+               int box_x, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)N * d * elem};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dtype, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr double kLog2e = 1.4426950408889634074;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const int BH = B * H;
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
+    return FA_ERR_LAUNCH;
+  a.lse = lse;
+  a.status = di->status;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = (float)((double)scale * kLog2e);
+  a.causal = causal ? 1 : 0;
+  return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const int BH = B * H;
+  const size_t rows = (size_t)BH * N;
+  fa::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.dqacc = static_cast<float*>(workspace);
+  a.Dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
+      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_dqacc, a.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 64))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq = dq;
+  a.status = di->status;
+  a.BH = BH;
+  a.N = N;
+  a.d = d;
+  a.scale = scale;
+  a.scale_log2 = (float)((double)scale * kLog2e);
+  a.causal = causal ? 1 : 0;
+  return fa::launch_bwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or device";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FA_ERR_LAUNCH: return "CUDA launch or query failed";
+    case FA_ERR_TIMEOUT: return "a kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_device_status(int reset) {
+  DeviceInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fa_device_status, sizeof(word)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (reset && word) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_device_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return word ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

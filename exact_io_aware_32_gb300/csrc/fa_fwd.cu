@@ -1,0 +1,330 @@
+// Forward pass of exact attention on sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and streams the
+// head's key/value blocks (128 rows each) past them, as in the blocked loop of
+// "FlashAttention and GPU Memory", chapter 07 (each SM takes one block of Q at
+// a time; blocks of K and V fly in; only O is written back). Per key block and
+// query tile:
+//   S = Q K^T                 tcgen05.mma, bf16 operands from shared memory,
+//                             fp32 accumulator in tensor memory (TMEM)
+//   m, l, P                   running row max / sum of exponentials (chapter
+//                             08), one TMEM lane (= one query row) per thread,
+//                             exponentials in base 2 with the scale folded in
+//   O += P V                  tcgen05.mma, P read back from TMEM as bf16
+// and at the end O / l and the row logsumexp are written.
+//
+// Warp roles (320 threads): warps 0-3 and 4-7 are the softmax/epilogue
+// warpgroups of query tiles 0 and 1, warp 8 issues TMA loads, warp 9 issues
+// the MMAs and owns the TMEM allocation. The two tiles alternate on the tensor
+// core so that one tile's softmax overlaps the other tile's products (the
+// staggering the pages describe for the third version, chapter 11).
+//
+// The running maximum used as the exponent reference is only moved when the
+// true row maximum exceeds it by more than 2^8; O and l are always scaled
+// against the same reference, so the final O / l is unchanged in exact
+// arithmetic while most O rescales are skipped.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace fa::ptx;
+
+constexpr float kLn2 = 0.693147180559945309417f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
+  static constexpr int BN = 128;                 // keys per block
+  static constexpr int kPanels = D / 64;         // 128-byte-wide column panels per row
+  static constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kPanels * kPanelBytes;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 reuses its first 64)
+  // and O_t (fp32, D columns) for query tiles t = 0, 1.
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
+  static constexpr int kThreads = 320;
+};
+
+struct FwdBarriers {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t teardown;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBarriers& bars = *reinterpret_cast<FwdBarriers*>(smem + C::kOffBar);
+  volatile int* abort_flag = &bars.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int bh = blockIdx.x;
+  const int qblk = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  const int nkv = (N + C::BN - 1) / C::BN;
+  int nb[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = qblk * 256 + t * 128;
+    nb[t] = r0 < N ? (CAUSAL ? min(r0 / C::BN + 1, nkv) : nkv) : 0;
+  }
+  const int nb_max = max(nb[0], nb[1]);
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.o_done[t], 1);
+    }
+    mbar_init(&bars.teardown, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full, pn * 64,
+                      qblk * 256 + t * 128, bh);
+      int nk_issued = 0, nv_issued = 0;
+      for (int j = 0; j < nb_max; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[s],
+                      pn * 64, j * C::BN, bh);
+        nk_issued = j + 1;
+        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[s],
+                      pn * 64, j * C::BN, bh);
+        nv_issued = j + 1;
+      }
+      // Let every issued copy land before the CTA can exit.
+      mbar_wait_drain(&bars.q_full, 0);
+      for (int i = max(0, nk_issued - C::kStages); i < nk_issued; ++i)
+        mbar_wait_drain(&bars.k_full[i % C::kStages], (i / C::kStages) & 1);
+      for (int i = max(0, nv_issued - C::kStages); i < nv_issued; ++i)
+        mbar_wait_drain(&bars.v_full[i % C::kStages], (i / C::kStages) & 1);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);  // Q, K both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);       // P from TMEM, V MN-major
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t k_base = smem_u32(smem + C::kOffK);
+      const uint32_t v_base = smem_u32(smem + C::kOffV);
+      bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
+      for (int j = 0; ok && j < nb_max; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!(ok = mbar_wait(&bars.k_full[s], ph, abort_flag))) break;
+        tc_fence_after();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nb[t]) continue;
+          // S_t aliases the P_t that the previous PV product reads: wait for it.
+          if (j > 0 && !(ok = mbar_wait(&bars.o_done[t], (j - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t d_s = tmem + C::col_s(t);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
+            mma_ss(d_s, sdesc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
+                   sdesc_sw128(k_base + s * C::kTileBytes + off, 16, 1024), kIdS, kk > 0);
+          }
+          mma_commit(&bars.s_full[t]);
+        }
+        if (!ok) break;
+        mma_commit(&bars.k_empty[s]);
+        if (!(ok = mbar_wait(&bars.v_full[s], ph, abort_flag))) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nb[t]) continue;
+          if (!(ok = mbar_wait(&bars.p_full[t], j & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t a_p = tmem + C::col_s(t);
+          const uint32_t d_o = tmem + C::col_o(t);
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_base + s * C::kTileBytes + kk * 2048, C::kPanelBytes, 1024),
+                   kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.o_done[t]);
+        }
+        if (!ok) break;
+        mma_commit(&bars.v_empty[s]);
+      }
+      mma_commit(&bars.teardown);
+      mbar_wait_drain(&bars.teardown, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
+    const int row = qblk * 256 + t * 128 + r;
+    const int nbt = nb[t];
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::col_s(t);
+    const uint32_t t_o = tmem + lane_off + C::col_o(t);
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY;  // exponent reference, log2 units of scaled scores
+    float l_sum = 0.f;        // sum of 2^(s * sl2 - m_ref) over the keys seen so far
+    bool ok = true;
+    for (int j = 0; j < nbt; ++j) {
+      ok = mbar_wait(&bars.s_full[t], j & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {  // keep the warp converged for the .sync.aligned ops below
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      const int kv0 = j * C::BN;
+      const bool need_mask = CAUSAL ? (j == nbt - 1) : (kv0 + C::BN > N);
+      if (need_mask) {
+        const int lim = CAUSAL ? (row - kv0) : (N - 1 - kv0);  // keep key column c iff c <= lim
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      float alpha = 1.f;
+      const bool move = m_new > m_ref + kRescaleThreshold;
+      if (move) {
+        alpha = ex2(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const bool rescale = __any_sync(0xffffffffu, move && j > 0);
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -m_ref));
+        const float p1 = ex2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, -m_ref));
+        sum0 += p0;
+        sum1 += p1;
+        pk[c >> 6][(c & 63) >> 1] = pack_bf16x2(p0, p1);
+      }
+      l_sum = l_sum * alpha + (sum0 + sum1);
+      tmem_st32(t_s, pk[0]);
+      tmem_st32(t_s + 32, pk[1]);
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(t_o + c, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[t]);
+    }
+    if (ok && nbt > 0) ok = mbar_wait(&bars.o_done[t], (nbt - 1) & 1, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (nbt > 0) {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
+      uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is no longer read by any MMA
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l_sum;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_ld_wait(o);
+          const int pn = c >> 6;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = ((c & 63) >> 3) + q4;  // 16-byte chunk within the 128-byte row
+            const uint32_t addr = smem_u32(stage + pn * C::kPanelBytes + r * 128 + ((chunk ^ (r & 7)) << 4));
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[q4 * 8 + i]) * inv_l;
+            st_shared_v4(addr, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                         pack_bf16x2(f[6], f[7]));
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (r == 0 && !*abort_flag) {
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_store_3d(&a.tm_o, stage + pn * C::kPanelBytes, pn * 64, qblk * 256 + t * 128, bh);
+        bulk_commit();
+        bulk_wait0();
+      }
+      if (ok && row < N) a.lse[(size_t)bh * N + row] = (m_ref + log2f(l_sum)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && bars.abort) atomicOr(a.status, 1u);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)a.BH, (unsigned)((a.N + 255) / 256));
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, int /*num_sms*/, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,40 @@
+// Internal interface between the C ABI shim (fa_api.cu) and the kernel
+// translation units. Host-only declarations; no CUDA types beyond CUtensorMap.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle
+  float* lse;                          // fp32 [BH][N]
+  unsigned int* status;                // device error word
+  int BH, N, d;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d]; q/dO box 64 x 64, k/v box 64 x 128
+  CUtensorMap tm_dqacc;                 // fp32 [BH][N][d], box 32 x 64, 128B swizzle (reduce-add)
+  CUtensorMap tm_dk, tm_dv;             // bf16 [BH][N][d], box 64 x 128 (stores)
+  const void* o;                        // bf16 [BH][N][d]
+  const void* dO;                       // bf16 [BH][N][d]
+  const float* lse;                     // fp32 [BH][N]
+  float* dqacc;                         // fp32 [BH][N][d]
+  float* Dsum;                          // fp32 [BH][N]
+  void* dq;                             // bf16 [BH][N][d]
+  unsigned int* status;
+  int BH, N, d;
+  float scale, scale_log2;
+  int causal;
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace fa

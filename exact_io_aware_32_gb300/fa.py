@@ -1,0 +1,151 @@
+"""Thin ctypes binding over libfa.so (include/fa.h).
+
+Argument marshalling only: every step of attention runs in the CUDA kernels
+of the library. The functions named like the C ABI (``fa_fwd``, ``fa_bwd``,
+``fa_bwd_workspace_bytes``, ``fa_status_string``, ``fa_device_status``) take
+either torch CUDA tensors or raw device addresses (ints). ``forward`` and
+``backward`` are conveniences that allocate the outputs with torch.
+
+If the library has not been built, or cannot be loaded, every call raises:
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_LAUNCH = 5
+FA_ERR_TIMEOUT = 6
+
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libfa.so (building it first if it is missing) and declare the signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            _build.build()
+        lib = ctypes.CDLL(p)
+        vp, c_int, c_float, c_size_t = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, vp]
+        lib.fa_fwd.restype = c_int
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, vp,
+                               c_size_t, vp]
+        lib.fa_bwd.restype = c_int
+        lib.fa_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
+        lib.fa_bwd_workspace_bytes.restype = c_size_t
+        lib.fa_status_string.argtypes = [c_int]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_device_status.argtypes = [c_int]
+        lib.fa_device_status.restype = c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+fa_status_string = status_string
+
+
+def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool, stream=None) -> int:
+    return int(load().fa_fwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), B, H, N, d, float(scale),
+                             int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+           workspace, workspace_bytes: int, stream=None) -> int:
+    return int(load().fa_bwd(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dO), _addr(dq), _addr(dk),
+                             _addr(dv), B, H, N, d, float(scale), int(bool(causal)), _addr(workspace),
+                             int(workspace_bytes), _stream(stream)))
+
+
+def fa_device_status(reset: bool = True) -> int:
+    return int(load().fa_device_status(int(bool(reset))))
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(s) for s in q.shape)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate o (bf16) and lse (fp32) with torch and run fa_fwd. Returns (o, lse)."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+    """Allocate dq, dk, dv (and the workspace if none is given) and run fa_bwd."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                workspace.numel() * workspace.element_size(), stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

@@ -1,0 +1,116 @@
+/*
+ * fa.h -- C ABI of the exact, IO-aware scaled-dot-product attention library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes. For every batch b and head h, with q, k, v the [N, d]
+ * slices of that head,
+ *     O = softmax(scale * q k^T [+ causal mask]) v
+ * exactly, not an approximation: the pages this follows state that the tiled
+ * method returns softmax(QK^T)V "with no approximation" and differs from a
+ * whole-matrix computation only by floating-point rounding
+ * ("FlashAttention does more arithmetic to move less data", section
+ * "FlashAttention never writes the full score table to HBM";
+ * "FlashAttention and GPU Memory", chapters 01, 08 and 12). The N x N score
+ * matrix never reaches device memory: score tiles live in on-chip tensor
+ * memory (chapter 07, "Blocks").
+ *
+ * The forward pass also returns one number per row, the natural-log
+ * logsumexp of the scaled, masked scores, which folds the running maximum m
+ * and running sum l that the method keeps per row (chapter 08, "A softmax with
+ * a running tally"; chapter 09 keeps "two numbers per row"). The backward
+ * pass rebuilds score tiles from q, k, v and that logsumexp instead of
+ * reading a stored probability matrix (chapter 09, "Backward: recomputing
+ * beats reading").
+ *
+ * Conventions shared by every call:
+ *   - q, k, v, o, dO, dq, dk, dv: bf16, contiguous [B, H, N, d], d innermost.
+ *   - lse: fp32, contiguous [B, H, N].
+ *   - Self-attention: queries and keys have the same length N.
+ *   - causal != 0 masks key j for query i when j > i (row 0 sees key 0 only).
+ *   - d must be 64 or 128. B, H, N >= 1, B * H * N * d < 2^31.
+ *   - scale must be finite and > 0 (usually 1 / sqrt(d)).
+ *   - Every pointer is a DEVICE pointer (the current CUDA device), 16-byte
+ *     aligned. The caller owns all memory; the library allocates no device
+ *     memory. Buffers must not overlap.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream). Calls
+ *     enqueue work and return without synchronising.
+ *   - Arguments are checked before anything is launched; on any error the
+ *     call returns a non-zero fa_status and leaves the outputs untouched.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, B/H/N < 1, size overflow, bad scale */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or no sm_100-family GPU */
+  FA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  FA_ERR_WORKSPACE = 4,   /* workspace pointer null or smaller than required */
+  FA_ERR_LAUNCH = 5,      /* the CUDA runtime rejected a launch or a query */
+  FA_ERR_TIMEOUT = 6      /* a kernel gave up waiting (reported by fa_device_status) */
+} fa_status;
+
+/*
+ * Forward pass (the tiled loop of chapter 07 with the running-max softmax of
+ * chapter 08, fused into one kernel that writes only o and lse).
+ *   q, k, v  [in]  bf16 [B, H, N, d]
+ *   o        [out] bf16 [B, H, N, d]
+ *   lse      [out] fp32 [B, H, N], lse[i] = ln sum_{j visible to i} exp(scale q_i . k_j)
+ * Returns FA_OK or an fa_status error code.
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
+ * accumulator [B, H, N, d] and the fp32 row terms D_i = dO_i . o_i [B, H, N],
+ * each padded to 256 bytes. Returns 0 if the shape is invalid.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass (chapter 09): gradients of a loss L with respect to q, k, v
+ * given dO = dL/dO, rebuilding each score tile from q, k and lse.
+ *   q, k, v, o, dO [in]  bf16 [B, H, N, d]  (o and lse from fa_fwd on the same q, k, v, scale, causal)
+ *   lse            [in]  fp32 [B, H, N]
+ *   dq, dk, dv     [out] bf16 [B, H, N, d]
+ *   workspace      [scratch] device memory of at least fa_bwd_workspace_bytes(B, H, N, d)
+ *                  bytes, 256-byte aligned; its contents on entry do not matter
+ *                  and are overwritten. It must not be used by another call
+ *                  that may run concurrently.
+ * dq is accumulated over key tiles with fp32 atomic adds, so its rounding can
+ * differ from run to run in the last bits; dk and dv are deterministic.
+ * Returns FA_OK or an fa_status error code.
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+FA_API const char* fa_status_string(int status);
+
+/*
+ * Reads (and, if reset != 0, clears) the device-side error word that kernels
+ * set when one of their internal waits exceeds its time limit, on the current
+ * device. Synchronises the device. Returns FA_OK, FA_ERR_TIMEOUT, or
+ * FA_ERR_LAUNCH if the word cannot be read.
+ */
+FA_API int fa_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

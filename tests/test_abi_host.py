@@ -1,0 +1,97 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports
+every function include/fa.h declares, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_32_gb300 import build, fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return re.findall(r"^FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def test_header_declares_expected_set():
+    assert set(declared_functions()) == set(fa.EXPORTED)
+
+
+def test_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(fa.lib_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for st in range(0, 7):
+        assert fa.status_string(st) and fa.status_string(st) != "unknown status"
+    assert fa.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    # fp32 dQ accumulator + fp32 D, each padded to 256 bytes
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 100 * 64 * 4 + ((2 * 3 * 100 * 4 + 255) // 256) * 256
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 128) == 512 + 256
+    assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
+
+
+A = 1 << 20  # a 16-byte aligned fake address; never dereferenced because validation fails first
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(k=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 4), fa.FA_ERR_MISALIGNED),
+])
+def test_fwd_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=16, d=64, scale=0.125, causal=0)
+    kw.update(args)
+    st = fa.fa_fwd(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["B"], kw["H"], kw["N"], kw["d"], kw["scale"],
+                   kw["causal"], stream=0)
+    assert st == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(dO=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(dq=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(ws=0), fa.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=100), fa.FA_ERR_WORKSPACE),
+    (dict(ws=A + 16), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=1, N=16, d=64, scale=0.125, causal=1,
+              ws=A, ws_bytes=1 << 20)
+    kw.update(args)
+    st = fa.fa_bwd(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["dO"], kw["dq"], kw["dk"], kw["dv"], kw["B"],
+                   kw["H"], kw["N"], kw["d"], kw["scale"], kw["causal"], kw["ws"], kw["ws_bytes"], stream=0)
+    assert st == status
+
+
+def test_no_gpu_reports_launch_error(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = fa.fa_fwd(A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, stream=0)
+    assert st == fa.FA_ERR_LAUNCH
