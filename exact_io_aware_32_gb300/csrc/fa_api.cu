@@ -151,13 +151,12 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   std::memset(&a, 0, sizeof(a));
   a.dqacc = static_cast<float*>(workspace);
   a.Dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
-  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
-      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_dqacc, a.dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BH, N, d, 32, 64))
+      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
     return FA_ERR_LAUNCH;
   a.o = o;
   a.dO = dO;

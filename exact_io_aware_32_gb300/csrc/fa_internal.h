@@ -18,9 +18,8 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d]; q/dO box 64 x 64, k/v box 64 x 128
-  CUtensorMap tm_dqacc;                 // fp32 [BH][N][d], box 32 x 64, 128B swizzle (reduce-add)
-  CUtensorMap tm_dk, tm_dv;             // bf16 [BH][N][d], box 64 x 128 (stores)
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (loads)
+  CUtensorMap tm_dk, tm_dv;             // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
   const void* o;                        // bf16 [BH][N][d]
   const void* dO;                       // bf16 [BH][N][d]
   const float* lse;                     // fp32 [BH][N]

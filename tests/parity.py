@@ -17,8 +17,16 @@ LSE_MAX_ABS = 1e-3
 GRAD_REL_RMS = 1e-2
 
 
+# Relative RMS divides by the reference's RMS; where the reference vanishes
+# (one key: dq = dk = 0 exactly) that RMS is floored at this absolute value,
+# so rounding noise of the order of bf16 epsilon times the inputs passes.
+RMS_FLOOR = 1e-3
+
+
 def rel_rms(x: np.ndarray, ref: np.ndarray) -> float:
-    return float(np.sqrt(((x - ref) ** 2).sum() / max(float((ref ** 2).sum()), 1e-300)))
+    n = max(ref.size, 1)
+    denom = max(float((ref ** 2).sum()), RMS_FLOOR ** 2 * n)
+    return float(np.sqrt(((x - ref) ** 2).sum() / denom))
 
 
 def to_np(t: torch.Tensor, shape) -> np.ndarray:
