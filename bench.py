@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward + backward on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one pass of the whole path over one batch: fa_fwd (O, lse) then
+fa_bwd (dq, dk, dv) on the same synthetic inputs. Under torchrun (N > 1) every
+rank runs the same per-GPU workload on its own inputs (heads are independent,
+so the work shards with no collective on the data path: weak scaling); the
+elapsed time is the maximum over ranks and ``value`` is the work of all ranks
+divided by it. Rank 0 prints one JSON line.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(rank 0 only; other ranks exit at once), each step a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_io_aware_32_gb300 import inputs, model  # noqa: E402
+
+METRIC = "attention fwd and fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 peak"
+DEFAULT_WORKLOAD = "d128_n4096_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+L2_BYTES = 129e6
+
+
+def workload_by_name(name: str):
+    """'<workload>_causal' / '<workload>_noncausal' -> (Workload, causal).
+
+    'custom_<B>_<H>_<N>_<d>_causal' (or _noncausal) names an ad-hoc shape with
+    the same input recipe, used for small profiling cases.
+    """
+    if name.startswith("custom_"):
+        parts = name.split("_")
+        B, H, N, d = (int(x) for x in parts[1:5])
+        causal = parts[5] == "causal"
+        return inputs.Workload(name, B, H, N, d, (causal,), seed=0), causal
+    for suffix, causal in (("_causal", True), ("_noncausal", False)):
+        if name.endswith(suffix):
+            w = inputs.WORKLOADS[name[: -len(suffix)]]
+            if causal not in w.causal:
+                raise SystemExit(f"{name}: that masking is not part of the workload")
+            return w, causal
+    raise SystemExit(f"unknown workload {name}; use <name>_causal or <name>_noncausal with name in "
+                     f"{sorted(inputs.WORKLOADS)}")
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(elapsed_s_per_rank, units_per_rank):
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    t = max(elapsed_s_per_rank)
+    return sum(units_per_rank) / t, t
+
+
+def reduce_max_over_ranks(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (identity without a process group)."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi missing"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w, causal: bool, rows: int, heads: int, threads: int):
+    """fwd + bwd of the fp64 oracle on the leading `rows` rows and keys of `heads` heads.
+
+    Returns (model flops of the sample, wall seconds). Under the causal mask the
+    leading rows and keys form a self-contained sub-problem; without it the
+    sample is the same arithmetic on a smaller square.
+    """
+    from oracle import oracle as orc
+
+    x = inputs.make_inputs(1, heads, rows, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    t0 = time.perf_counter()
+    orc.fwd(x["q"], x["k"], x["v"], w.softmax_scale, causal, nthreads=threads)
+    orc.bwd(x["q"], x["k"], x["v"], x["dO"], w.softmax_scale, causal, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = model.fwd_flops(1, heads, rows, w.d, causal) + model.bwd_flops(1, heads, rows, w.d, causal)
+    return flops, dt
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, causal: bool, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on whole heads of the workload until the budget is spent."""
+    from oracle import oracle as orc
+
+    cores = host_cores()
+    threads = orc.max_threads(cores)
+    flops = secs = 0.0
+    heads = 0
+    while heads < w.BH and secs < budget_s:
+        f, s = oracle_sample(w, causal, w.N, 1, threads)
+        flops += f
+        secs += s
+        heads += 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{heads} of {w.BH} heads at full N={w.N}, d={w.d}, fwd+bwd, fp64, "
+                      f"{secs:.1f} s wall; flops by the same matmul-only convention"}
+
+
+# ---------------------------------------------------------------------- GPU arm
+def kernel_traffic(source: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    with open(os.path.join(ROOT, "exact_io_aware_32_gb300", "csrc", source), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    e = entries.get(kernel)
+    if not e or e.get("source_sha256") != sha:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_gpu(args, w, causal: bool):
+    import torch
+
+    from exact_io_aware_32_gb300 import fa
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = w.softmax_scale
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 * w.seed + rank)
+    shape = (B, H, N, d)
+
+    def draw(mult=1.0):
+        t = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if mult != 1.0:
+            t.mul_(mult)
+        return t.to(torch.bfloat16)
+
+    q, k, v = draw(w.qk_mult), draw(w.qk_mult), draw()
+    dO = draw()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = int(stream.cuda_stream)
+
+    def fwd():
+        st = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, sp)
+        if st:
+            raise fa.FAError(st, "fa_fwd")
+
+    def bwd():
+        st = fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, sp)
+        if st:
+            raise fa.FAError(st, "fa_bwd")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    barrier()
+    st = fa.fa_device_status(True)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.4)  # let the sampler start before the timed region
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fwd()
+        e1.record(stream)
+        bwd()
+        e2.record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    fwd_s = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / 1e3 / args.steps
+    bwd_s = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / 1e3 / args.steps
+    st = fa.fa_device_status(True)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "timed region")
+
+    f_fwd = model.fwd_flops(B, H, N, d, causal)
+    f_bwd = model.bwd_flops(B, H, N, d, causal)
+    units = (f_fwd + f_bwd) * args.steps
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, dO))
+    ho, hlse = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(q, device="cpu").pin_memory() for _ in range(3))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        for dst, src in ((q, hq), (k, hk), (v, hv), (dO, hdo)):
+            dst.copy_(src, non_blocking=True)
+        fwd()
+        bwd()
+        for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    barrier()
+    e2e_elapsed = a0.elapsed_time(a1) / 1e3
+
+    elapsed, e2e_elapsed, fwd_s, bwd_s = reduce_max_over_ranks([elapsed, e2e_elapsed, fwd_s, bwd_s], dist, dev)
+
+    value, _ = aggregate([elapsed], [units * world])
+    e2e_value = (f_fwd + f_bwd) * e2e_steps * world / e2e_elapsed
+    peaks = measured_peaks()
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
+    achieved = f_bwd / bwd_s / 1e12
+    traffic = kernel_traffic("fa_bwd.cu", f"fa_bwd_main_kernel<{d},{str(causal).lower()}>")
+    result = {
+        "metric": METRIC,
+        "value": round(value / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+            "scale": scale, "qk_mult": w.qk_mult,
+            "step": "fa_fwd then fa_bwd (O, lse, dq, dk, dv)",
+            "parallelism": f"replicas over (batch, head): {world} x {B * H} heads",
+            "l2": f"inputs larger than L2: {5 * B * H * N * d * 2 / 1e6:.0f} MB of bf16 tensors per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
+            "flops_per_step": f_fwd + f_bwd,
+        },
+        "fwd": {"ms": round(fwd_s * 1e3, 4), "tflops": round(f_fwd / fwd_s / 1e12, 2),
+                "pct_of_peak": round(100 * f_fwd / fwd_s / 1e12 / burst, 2)},
+        "bwd": {"ms": round(bwd_s * 1e3, 4), "tflops": round(achieved, 2),
+                "pct_of_peak": round(100 * achieved / burst, 2)},
+        "pct_of_peak": round(100 * value / 1e12 / world / burst, 2),
+        "peak_basis": f"{peaks['source']} dense bf16 burst {burst} TFLOP/s per GPU",
+        "roofline": {
+            "kernel": "fa_bwd (prep + main + dq cast; main dominates)",
+            "bound": "tensor", "achieved": round(achieved, 2), "peak": sustained, "unit": "TFLOP/s",
+            "frac": round(achieved / sustained, 4), "traffic": traffic,
+            "peak_basis": f"{peaks['source']} sustained dense bf16 (kernel timed inside a long step)",
+            "algorithmic_flops_per_launch": f_bwd,
+        },
+        "e2e": {"value": round(e2e_value / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, causal, args.cpu_budget)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args, w, causal: bool):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+
+    cores = host_cores()
+    threads = orc.max_threads(cores)
+    # size each step's sample so the whole run stays within a few minutes
+    f0, s0 = oracle_sample(w, causal, 512, 1, threads)
+    speed = f0 / s0
+    per_step = min(1.0, args.reference_budget / max(1, args.steps + args.warmup))
+    per_row2 = (model.fwd_flops(1, 1, 1, w.d, causal) + model.bwd_flops(1, 1, 1, w.d, causal))
+    rows = int(math.sqrt(per_step * speed / per_row2)) // 64 * 64
+    rows = max(64, min(w.N, rows))
+    for _ in range(args.warmup):
+        oracle_sample(w, causal, rows, 1, threads)
+    flops = secs = 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(w, causal, rows, 1, threads)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    sample = (f"per step: leading {rows} rows and keys of one head of the workload (N={w.N}, d={w.d}), "
+              f"fwd+bwd, fp64")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--reference-budget", type=float, default=120.0, help="seconds for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w, causal = workload_by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, causal)
+    else:
+        run_gpu(args, w, causal)
+
+
+if __name__ == "__main__":
+    main()
