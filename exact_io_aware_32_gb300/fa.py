@@ -2,7 +2,8 @@
 
 Argument marshalling only: every step of attention runs in the CUDA kernels
 of the library. The functions named like the C ABI (``fa_fwd``, ``fa_bwd``,
-``fa_bwd_workspace_bytes``, ``fa_status_string``, ``fa_device_status``) take
+``fa_bwd_workspace_bytes``, ``fa_status_string``, ``fa_device_status``,
+``fa_bwd_noalloc``) take
 either torch CUDA tensors or raw device addresses (ints). ``forward`` and
 ``backward`` are conveniences that allocate the outputs with torch.
 
@@ -26,7 +27,7 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status")
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -149,3 +150,27 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
     return dq, dk, dv
+
+
+# Largest scratch fa_bwd_noalloc holds per device (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES in include/fa.h).
+FA_BWD_NOALLOC_MAX_SCRATCH_BYTES = 32 << 20
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                   stream=None) -> int:
+    """fa_bwd without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps the scratch in a fixed device array of
+    FA_BWD_NOALLOC_MAX_SCRATCH_BYTES; larger shapes return FA_ERR_WORKSPACE.
+    The first call on a device looks up that array's address, so make it
+    before any stream capture; calls that may overlap on one device race on
+    the shared array.
+    """
+    lib = load()
+    fn = lib.fa_bwd_noalloc
+    if fn.argtypes is None:
+        vp, c_int, c_float = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, vp]
+        fn.restype = c_int
+    return int(fn(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dO), _addr(dq), _addr(dk), _addr(dv),
+                  B, H, N, d, float(scale), int(bool(causal)), _stream(stream)))

@@ -98,6 +98,39 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
            size_t workspace_bytes, void* stream);
 
+/*
+ * Largest scratch, in bytes, that fa_bwd_noalloc holds per device: the
+ * shapes it accepts are those with fa_bwd_workspace_bytes(B, H, N, d) <= this
+ * (B * H * N up to 65,027 rows at d = 128, or 129,055 at d = 64).
+ */
+#define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * Backward pass for callers that cannot allocate device memory. The pages
+ * have no counterpart to this call; it exists for callers that are given no
+ * allocator (a plug-in inside a host framework that owns all device memory) or
+ * may not call cudaMalloc (a latency-critical path that cannot afford its
+ * implicit synchronisation).
+ *
+ * Same arguments, results and errors as fa_bwd, without the workspace: the
+ * scratch lives in a fixed FA_BWD_NOALLOC_MAX_SCRATCH_BYTES device array
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits. The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   - Shapes whose scratch need exceeds the maximum are rejected with
+ *     FA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current). Make that first call
+ *     on a device before any stream capture begins.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents (the call itself zeroes what must start at zero). Calls
+ *     that may overlap on the GPU, e.g. on two streams of one device, race on
+ *     it: order them on one stream or synchronise between them.
+ */
+FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                          int causal, void* stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);
 
