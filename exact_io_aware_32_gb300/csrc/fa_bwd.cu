@@ -17,9 +17,11 @@
 // bwd_main warp roles (320 threads): warps 0-3 (warpgroup 0) turn S^T and dP^T
 // into P^T (written back to tensor memory as bf16) and dS^T (written to shared
 // memory as bf16); warps 4-7 (warpgroup 1) drain each dQ block from tensor
-// memory into the fp32 accumulator with vector atomic adds; warp 8 issues TMA
-// loads; warp 9 issues the tcgen05 MMAs. Thread r of a warpgroup owns TMEM
-// lane r: key r of the block for S^T, dP^T, dK, dV; query r for dQ.
+// memory into the fp32 accumulator with atomic adds; warp 8 issues TMA loads;
+// warp 9 issues the tcgen05 MMAs. Thread r of a warpgroup owns TMEM lane r:
+// key r of the block for S^T, dP^T, dK, dV; for the dQ block, feature r at
+// d = 128 (the product is formed transposed, dQ^T = K^T dS^T, so that a warp's
+// atomics hit one contiguous row) and query r at d = 64.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -56,11 +58,15 @@ struct BwdCfg {
 struct BwdBarriers {
   uint64_t kv_full;
   uint64_t qd_full[2], qd_empty[2];
-  uint64_t s_full, dp_full, ds_ready, mma_done, dq_free;
+  uint64_t s_full, dp_full, ds_ready, dq_full, mma_done, dq_free;
   uint64_t teardown;
   uint32_t tmem_base;
   int abort;
 };
+
+__device__ __forceinline__ void red_add_f32(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_ready, 128);
+    mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.teardown, 1);
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV: P^T from TMEM, dO MN-major
       constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dK: dS^T K-major, Q MN-major
-      constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: dS MN-major, K MN-major
+      constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ (or dQ^T): both operands MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
       const uint32_t ds_base = smem_u32(smem + C::kOffDS);
@@ -187,6 +194,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
         mma_commit(&bars.dp_full);
         if (!(ok = mbar_wait(&bars.ds_ready, it & 1, abort_flag))) break;
         tc_fence_after();
+        if (D == 64 && it > 0 && !(ok = mbar_wait(&bars.dq_free, (it - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        // dQ first, so that its drain overlaps dV and dK. K = 128 keys.
+        // d = 128: dQ^T = K^T dS^T (lane = feature), so the drain's atomics are
+        //          contiguous along d; d = 64: dQ = dS K (lane = query).
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk) {
+          const uint64_t dsd = sdesc_sw128(ds_base + kk * 2048, C::kPanelBytes, 1024);
+          const uint64_t kd = sdesc_sw128(k_base + kk * 2048, C::kPanelBytes, 1024);
+          if (D == 128)
+            mma_ss(tmem + C::kColDQ, kd, dsd, kIdMM, kk > 0);
+          else
+            mma_ss(tmem + C::kColDQ, dsd, kd, kIdMM, kk > 0);
+        }
+        mma_commit(&bars.dq_full);
         // dV += P^T dO_i   (K = 128 queries, 16 per instruction)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
@@ -199,13 +221,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
           mma_ss(tmem + C::kColDK, sdesc_sw128(ds_base + off, 16, 1024),
                  sdesc_sw128(qs + kk * 2048, C::kPanelBytes, 1024), kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
-        if (D == 64 && it > 0 && !(ok = mbar_wait(&bars.dq_free, (it - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        // dQ_i = dS K_j   (K = 128 keys)
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(ds_base + kk * 2048, C::kPanelBytes, 1024),
-                 sdesc_sw128(k_base + kk * 2048, C::kPanelBytes, 1024), kIdMM, kk > 0);
         mma_commit(&bars.mma_done);
         mma_commit(&bars.qd_empty[s]);
       }
@@ -322,30 +337,49 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_main_kernel(const __grid_consta
     const float scale = a.scale;
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
-      ok = mbar_wait(&bars.mma_done, it & 1, abort_flag);
+      ok = mbar_wait(&bars.dq_full, it & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int q = (i_start + it) * C::BQ + r;
-      float* dst = a.dqacc + ((size_t)bh * N + q) * D;
+      const int q0 = (i_start + it) * C::BQ;
+      if (D == 128) {
+        // lane r = feature r; columns = the block's 128 queries. Each warp adds
+        // 32 consecutive floats of one dQ row per instruction.
+        float* col = a.dqacc + ((size_t)bh * N + q0) * D + r;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::kColDQ + c, o);
-        tmem_ld_wait(o);
-        if (q < N) {
+        for (int c0 = 0; c0 < C::BQ; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + C::kColDQ + c0, o);
+          tmem_ld_wait(o);
+          const int nvalid = min(32, N - (q0 + c0));
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            red_add_v4(dst + c + i, __uint_as_float(o[i]) * scale, __uint_as_float(o[i + 1]) * scale,
-                       __uint_as_float(o[i + 2]) * scale, __uint_as_float(o[i + 3]) * scale);
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) red_add_f32(col + (size_t)(c0 + i) * D, __uint_as_float(o[i]) * scale);
+        }
+      } else {
+        const int q = q0 + r;  // lane r = query r
+        float* dst = a.dqacc + ((size_t)bh * N + q) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + C::kColDQ + c, o);
+          tmem_ld_wait(o);
+          if (q < N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(dst + c + i, __uint_as_float(o[i]) * scale, __uint_as_float(o[i + 1]) * scale,
+                         __uint_as_float(o[i + 2]) * scale, __uint_as_float(o[i + 3]) * scale);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&bars.dq_free);
     }
-    // dK epilogue (the last mma_done phase was consumed by the loop above)
+    if (ok && n_iter > 0) ok = mbar_wait(&bars.mma_done, (n_iter - 1) & 1, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    // dK epilogue, once the last products have completed
     uint8_t* stage = smem + C::kOffDO;
     if (ok && n_iter > 0) {
       tc_fence_after();

@@ -153,43 +153,58 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       const uint32_t k_base = smem_u32(smem + C::kOffK);
       const uint32_t v_base = smem_u32(smem + C::kOffV);
-      bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
+      auto issue_s = [&](int t, int st) {
+        const uint32_t d_s = tmem + C::col_s(t);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
+          mma_ss(d_s, sdesc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
+                 sdesc_sw128(k_base + st * C::kTileBytes + off, 16, 1024), kIdS, kk > 0);
+        }
+        mma_commit(&bars.s_full[t]);
+      };
+      bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.k_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nb[t] > 0) issue_s(t, 0);
+        mma_commit(&bars.k_empty[0]);
+      }
+      // Per key block j and tile t: O_t += P_t V_j, then at once S_t for block
+      // j + 1. S_t(j + 1) overwrites the columns P_t(j) occupies; the products
+      // of one thread execute in issue order, so PV_t(j) has read P_t(j)
+      // before S_t(j + 1) writes them, and when S_t(j + 1) completes, so has
+      // PV_t(j) (the softmax may then rescale O_t).
       for (int j = 0; ok && j < nb_max; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
-        if (!(ok = mbar_wait(&bars.k_full[s], ph, abort_flag))) break;
-        tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nb[t]) continue;
-          // S_t aliases the P_t that the previous PV product reads: wait for it.
-          if (j > 0 && !(ok = mbar_wait(&bars.o_done[t], (j - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t d_s = tmem + C::col_s(t);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
-            mma_ss(d_s, sdesc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
-                   sdesc_sw128(k_base + s * C::kTileBytes + off, 16, 1024), kIdS, kk > 0);
-          }
-          mma_commit(&bars.s_full[t]);
-        }
-        if (!ok) break;
-        mma_commit(&bars.k_empty[s]);
         if (!(ok = mbar_wait(&bars.v_full[s], ph, abort_flag))) break;
+        const int jn = j + 1, sn = jn % C::kStages;
+        bool k_next = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nb[t]) continue;
-          if (!(ok = mbar_wait(&bars.p_full[t], j & 1, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t a_p = tmem + C::col_s(t);
-          const uint32_t d_o = tmem + C::col_o(t);
+          if (j < nb[t]) {
+            if (!(ok = mbar_wait(&bars.p_full[t], j & 1, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t a_p = tmem + C::col_s(t);
+            const uint32_t d_o = tmem + C::col_o(t);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_base + s * C::kTileBytes + kk * 2048, C::kPanelBytes, 1024),
-                   kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.o_done[t]);
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+              mma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_base + s * C::kTileBytes + kk * 2048, C::kPanelBytes, 1024),
+                     kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.o_done[t]);
+          }
+          if (jn < nb[t]) {
+            if (!k_next) {
+              if (!(ok = mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, abort_flag))) break;
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, sn);
+          }
         }
         if (!ok) break;
         mma_commit(&bars.v_empty[s]);
+        if (k_next) mma_commit(&bars.k_empty[sn]);
       }
       mma_commit(&bars.teardown);
       mbar_wait_drain(&bars.teardown, 0);
