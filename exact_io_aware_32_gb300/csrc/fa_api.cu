@@ -128,7 +128,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
   const size_t rows = (size_t)B * H * N;
-  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+  return align256(rows * sizeof(float));
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -146,22 +146,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   const int BH = B * H;
-  const size_t rows = (size_t)BH * N;
   fa::BwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.dqacc = static_cast<float*>(workspace);
-  a.Dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
+  a.Dsum = static_cast<float*>(workspace);
   if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
     return FA_ERR_LAUNCH;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
-  a.dq = dq;
   a.status = di->status;
   a.BH = BH;
   a.N = N;

@@ -4,8 +4,7 @@
 // hands out no allocator, or code on a latency-critical path where a
 // cudaMalloc (with its implicit synchronisation and unpredictable cost) is not
 // allowed. For them this entry point keeps the backward pass's scratch (the
-// fp32 dQ accumulator and the fp32 row terms D) in a fixed array inside the
-// library. It calls no cudaMalloc, cudaFree or any allocating routine.
+// fp32 row terms D) in a fixed array inside the library. It calls no cudaMalloc, cudaFree or any allocating routine.
 //
 // The array is a file-scope __device__ variable, so each GPU that loads this
 // code holds kFaBwdNoallocMaxScratch bytes of it until the process exits.
@@ -60,8 +59,8 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   if (need == 0 || need > kFaBwdNoallocMaxScratch) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if ((st = scratch_on_current_device(&scratch)) != FA_OK) return st;
-  // The backward pass zeroes the dQ accumulator and rewrites D itself, so the
-  // previous call's contents of the scratch do not matter.
+  // The backward pass writes every scratch value (the row terms D) before it
+  // reads it, so the previous call's contents do not matter.
   return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, scratch, kFaBwdNoallocMaxScratch,
                 stream);
 }

@@ -19,13 +19,11 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (loads)
-  CUtensorMap tm_dk, tm_dv;             // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
+  CUtensorMap tm_dq, tm_dk, tm_dv;      // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
   const void* o;                        // bf16 [BH][N][d]
   const void* dO;                       // bf16 [BH][N][d]
   const float* lse;                     // fp32 [BH][N]
-  float* dqacc;                         // fp32 [BH][N][d]
-  float* Dsum;                          // fp32 [BH][N]
-  void* dq;                             // bf16 [BH][N][d]
+  float* Dsum;                          // fp32 [BH][N], in the caller's workspace
   unsigned int* status;
   int BH, N, d;
   float scale, scale_log2;

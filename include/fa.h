@@ -74,9 +74,9 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            float scale, int causal, void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for this shape: an fp32 dQ
- * accumulator [B, H, N, d] and the fp32 row terms D_i = dO_i . o_i [B, H, N],
- * each padded to 256 bytes. Returns 0 if the shape is invalid.
+ * Bytes of device workspace fa_bwd needs for this shape: the fp32 row terms
+ * D_i = dO_i . o_i [B, H, N], padded to 256 bytes. Returns 0 if the shape is
+ * invalid.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -90,8 +90,8 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                  bytes, 256-byte aligned; its contents on entry do not matter
  *                  and are overwritten. It must not be used by another call
  *                  that may run concurrently.
- * dq is accumulated over key tiles with fp32 atomic adds, so its rounding can
- * differ from run to run in the last bits; dk and dv are deterministic.
+ * dq, dk and dv are each summed on chip in a fixed order: repeated calls on
+ * the same inputs give bit-identical results.
  * Returns FA_OK or an fa_status error code.
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -101,7 +101,7 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
 /*
  * Largest scratch, in bytes, that fa_bwd_noalloc holds per device: the
  * shapes it accepts are those with fa_bwd_workspace_bytes(B, H, N, d) <= this
- * (B * H * N up to 65,027 rows at d = 128, or 129,055 at d = 64).
+ * (B * H * N up to 8,388,608 rows).
  */
 #define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -123,7 +123,7 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
  *     (cudaGetSymbolAddress, with that device current). Make that first call
  *     on a device before any stream capture begins.
  *   - Every call on a device shares the one array, which keeps the previous
- *     call's contents (the call itself zeroes what must start at zero). Calls
+ *     call's contents (each call writes every value it later reads). Calls
  *     that may overlap on the GPU, e.g. on two streams of one device, race on
  *     it: order them on one stream or synchronise between them.
  */

@@ -48,7 +48,7 @@ def test_bwd_single_head_workload(causal):
 
 
 def test_bwd_workspace_contents_do_not_matter():
-    """The workspace is overwritten: garbage on entry gives the same gradients (up to dq atomics order)."""
+    """The workspace is overwritten: garbage on entry gives bit-identical gradients."""
     B, H, N, d = 1, 2, 300, 128
     x, g = parity.gpu_inputs(B, H, N, d, seed=77)
     o, lse = fa.forward(g["q"], g["k"], g["v"], causal=True)
@@ -58,8 +58,8 @@ def test_bwd_workspace_contents_do_not_matter():
     ws.fill_(0xFF)  # NaN bit patterns everywhere
     r2 = fa.backward(g["q"], g["k"], g["v"], o, lse, g["dO"], causal=True, workspace=ws)
     parity.check_status()
-    assert torch.equal(r1[1], r2[1]) and torch.equal(r1[2], r2[2])  # dk, dv deterministic
-    assert (r1[0].float() - r2[0].float()).abs().max().item() <= 1e-2
+    for a, b in zip(r1, r2):  # dq, dk, dv are summed in a fixed order
+        assert torch.equal(a, b)
     assert torch.isfinite(r2[0].float()).all()
 
 

@@ -34,12 +34,12 @@ def test_noalloc_matches_workspace_backward_twice(B, H, N, d, causal):
             a, b = parity.to_np(got, shape), parity.to_np(want, shape)
             err = parity.rel_rms(a, b)
             assert err <= parity.GRAD_REL_RMS, (call, name, err)
-        # dk and dv involve no atomics: identical to the workspace version
-        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+        # the pass is deterministic: identical to the workspace version
+        assert torch.equal(dq, ref[0]) and torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
 
 
 def test_noalloc_rejects_shape_beyond_scratch():
-    B, H, N, d = 1, 1, 70000, 128  # 70000 rows need more than the 32 MiB built-in scratch
+    B, H, N, d = 1, 1, 9_000_000, 64  # 9 M rows need more than the 32 MiB built-in scratch
     assert fa.fa_bwd_workspace_bytes(B, H, N, d) > fa.FA_BWD_NOALLOC_MAX_SCRATCH_BYTES
     t = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((B, H, N), dtype=torch.float32, device="cuda")
