@@ -23,9 +23,12 @@
 // Warp roles in both main kernels (320 threads): warpgroups 0 and 1 (warps
 // 0-7) do the elementwise work, each on half of the block's columns (thread r
 // owns TMEM lane r); warp 8 issues TMA loads; warp 9 issues the tcgen05 MMAs
-// and owns the 512-column TMEM allocation. P^T (dK/dV kernel) and dS (dQ
-// kernel) are written back into TMEM as bf16 over the fp32 columns they came
-// from and used from there as the A operand of the next product.
+// and owns the 512-column TMEM allocation. P^T and dS^T (dK/dV kernel) and dS
+// (dQ kernel) are written back into TMEM as bf16 over fp32 columns the
+// warpgroups have already read, and used from there as the A operand of the
+// next product. Each S or dP tile is released to the MMA warp as soon as the
+// warpgroups hold it in registers, so the next tile's product overlaps their
+// elementwise work.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -71,6 +74,9 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t taddr, uint8_t* tile, in
 }
 
 // ============================================================================ dK / dV
+// One CTA per 128-key block (TMEM lane = key), 128 queries per iteration.
+// Warpgroup w handles queries [64 w, 64 w + 64) of each block and writes P^T
+// and dS^T (bf16) over its own dP^T columns once it has read them.
 template <int D>
 struct DkdvCfg {
   static constexpr int BK = 128;  // keys per CTA
@@ -83,8 +89,9 @@ struct DkdvCfg {
   static constexpr int kOffRow = 6 * kTileBytes;  // [parity][warpgroup][lse(64) | D(64)] fp32
   static constexpr int kOffBar = kOffRow + 2 * 2 * 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr uint32_t kColS = 0;    // S^T fp32; P^T bf16 in [0,32) and [64,96)
-  static constexpr uint32_t kColDP = 128;  // dP^T fp32; dS^T bf16 in [128,160) and [192,224)
+  static constexpr uint32_t kColS = 0;     // S^T fp32
+  static constexpr uint32_t kColDP = 128;  // dP^T fp32; warpgroup w then writes P^T (bf16) over its
+                                           // columns [128 + 64 w, +32) and dS^T over [+32, +64)
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
 };
@@ -92,10 +99,21 @@ struct DkdvCfg {
 struct DkdvBarriers {
   uint64_t kv_full;
   uint64_t qd_full[2], qd_empty[2];
-  uint64_t s_full, dp_full, ds_ready, mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, ds_ready, mma_done, teardown;
   uint32_t tmem_base;
   int abort;
 };
+
+// TMEM column, relative to the dP^T columns, of the packed bf16 operand for
+// k-step kk (16 queries): warpgroup w holds queries [64 w, 64 w + 64) with P^T
+// at [64 w, 64 w + 32) and dS^T at [64 w + 32, 64 w + 64).
+__device__ __forceinline__ uint32_t dkdv_pcol(int kk, bool ds) {
+  return (uint32_t)(64 * (kk >> 2) + (ds ? 32 : 0) + 8 * (kk & 3));
+}
+
+// Shared-memory descriptors address the operand start in bits [0,14) as
+// (address >> 4); moving within the same smem window adds to that field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
@@ -122,6 +140,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       mbar_init(&bars.qd_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.mma_done, 1);
@@ -171,40 +190,64 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV, dK: A from TMEM, B MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
-      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag);
-      // S^T and dP^T of block i+1 are issued right after dV and dK of block i;
-      // the products of one thread execute in issue order, so dV and dK have
-      // read P^T and dS^T before the next S^T and dP^T overwrite them.
+      // Descriptors for stage 0; stage 1 adds kTileBytes.
+      uint64_t dk_[D / 16], dv_[D / 16], dq_[D / 16], ddo_[D / 16], dqm[C::BQ / 16], ddom[C::BQ / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
+        dv_[kk] = sdesc_sw128(v_base + off, 16, 1024);
+        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
+        ddo_[kk] = sdesc_sw128(do_base + off, 16, 1024);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::BQ / 16; ++kk) {
+        dqm[kk] = sdesc_sw128(q_base + kk * 2048, kPanelBytes, 1024);
+        ddom[kk] = sdesc_sw128(do_base + kk * 2048, kPanelBytes, 1024);
+      }
+      auto issue_s = [&](int it) -> bool {  // S^T = K Q_i^T
+        const int s = it & 1;
+        if (!mbar_wait(&bars.qd_full[s], (it >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t so = s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColS, dk_[kk], desc_add(dq_[kk], so), kIdKK, kk > 0);
+        mma_commit(&bars.s_full);
+        return true;
+      };
+      auto issue_dp = [&](int it) {  // dP^T = V dO_i^T (dO_i is in the stage S^T of block i waited for)
+        const uint32_t so = (it & 1) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, dv_[kk], desc_add(ddo_[kk], so), kIdKK, kk > 0);
+        mma_commit(&bars.dp_full);
+      };
+      // S^T of block i+1 is issued as soon as both warpgroups have read S^T of
+      // block i, so it overlaps their elementwise work. dP^T of block i+1
+      // follows dV and dK of block i in issue order: the products of one
+      // thread execute in that order, so dV and dK have read P^T and dS^T
+      // before dP^T overwrites the columns that hold them.
+      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag) && issue_s(0);
+      if (ok) issue_dp(0);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it & 1;
-        const uint32_t qs = q_base + s * C::kTileBytes, dos = do_base + s * C::kTileBytes;
-        if (!(ok = mbar_wait(&bars.qd_full[s], (it >> 1) & 1, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024), kIdKK,
-                 kk > 0);
+        const uint32_t so = s * C::kTileBytes;
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait(&bars.s_free, it & 1, abort_flag))) break;
+          if (!(ok = issue_s(it + 1))) break;
         }
-        mma_commit(&bars.s_full);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(dos + off, 16, 1024), kIdKK,
-                 kk > 0);
-        }
-        mma_commit(&bars.dp_full);
         if (!(ok = mbar_wait(&bars.ds_ready, it & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(kk),
-                 sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024), kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), desc_add(ddom[kk], so), kIdTS,
+                 (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(kk),
-                 sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), desc_add(dqm[kk], so), kIdTS,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.qd_empty[s]);
+        if (it + 1 < n_iter) issue_dp(it + 1);
       }
       mma_commit(&bars.mma_done);
       mma_commit(&bars.teardown);
@@ -218,7 +261,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const int key = kblk * C::BK + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS + 64 * w;
-    const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;
+    const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;  // dP^T, then P^T | dS^T (bf16)
     const float sl2 = a.scale_log2;
     const bool key_ok = key < N;
     // Threads 0-63 of the warpgroup fetch lse (log2 units) of the group's 64
@@ -236,6 +279,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       rb[tt] = next;
       named_bar_sync(1 + w, 128);
       if (it + 1 < n_iter) next = fetch(it + 1);
+      const float4* rb4 = reinterpret_cast<const float4*>(rb);  // lse at [0, 64), D at [64, 128)
       ok = mbar_wait(&bars.s_full, it & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -244,24 +288,33 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       tc_fence_after();
       uint32_t pk[32];  // P^T row r, queries 64 w .. 64 w + 63, as bf16 pairs
       {
-        const bool diag = CAUSAL && (q0 == kblk * C::BK);
+        uint32_t sr[2][32];
+        tmem_ld32(t_s, sr[0]);
+        tmem_ld32(t_s + 32, sr[1]);
+        tmem_ld_wait(sr[0]);
+        tmem_ld_wait(sr[1]);
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
+        // causal: query q0 + 64 w + col sees key kblk * BK + r only if q0 + 64 w + col >= key
+        const int lim = CAUSAL ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t sr[32];
-          tmem_ld32(t_s + 32 * h, sr);
-          tmem_ld_wait(sr);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
+          for (int c = 0; c < 32; c += 4) {
             const int col = 32 * h + c;  // within the group's 64 queries
-            float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -rb[col]));
-            float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -rb[col + 1]));
-            // causal diagonal block: query q0 + 64 w + col sees key q0 + r only if 64 w + col >= r
-            if ((diag && 64 * w + col < r) || !key_ok) p0 = 0.f;
-            if ((diag && 64 * w + col + 1 < r) || !key_ok) p1 = 0.f;
+            const float4 l4 = rb4[col >> 2];
+            float p0 = ex2(fmaf(__uint_as_float(sr[h][c]), sl2, -l4.x));
+            float p1 = ex2(fmaf(__uint_as_float(sr[h][c + 1]), sl2, -l4.y));
+            float p2 = ex2(fmaf(__uint_as_float(sr[h][c + 2]), sl2, -l4.z));
+            float p3 = ex2(fmaf(__uint_as_float(sr[h][c + 3]), sl2, -l4.w));
+            if (col < lim || !key_ok) p0 = 0.f;
+            if (col + 1 < lim || !key_ok) p1 = 0.f;
+            if (col + 2 < lim || !key_ok) p2 = 0.f;
+            if (col + 3 < lim || !key_ok) p3 = 0.f;
             pk[col >> 1] = pack_bf16x2(p0, p1);
+            pk[(col >> 1) + 1] = pack_bf16x2(p2, p3);
           }
         }
-        tmem_st32(t_s, pk);  // over S^T columns this warpgroup has read
       }
       ok = mbar_wait(&bars.dp_full, it & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -270,22 +323,28 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       }
       tc_fence_after();
       {
-        uint32_t dsk[32];
+        uint32_t dp[2][32], dsk[32];
+        tmem_ld32(t_dp, dp[0]);
+        tmem_ld32(t_dp + 32, dp[1]);
+        tmem_ld_wait(dp[0]);
+        tmem_ld_wait(dp[1]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t dp[32];
-          tmem_ld32(t_dp + 32 * h, dp);
-          tmem_ld_wait(dp);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
+          for (int c = 0; c < 32; c += 4) {
             const int col = 32 * h + c;
-            const uint32_t pp = pk[col >> 1];
-            const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(dp[c]) - rb[64 + col]);
-            const float d1 = __uint_as_float(pp & 0xFFFF0000u) * (__uint_as_float(dp[c + 1]) - rb[64 + col + 1]);
+            const float4 d4 = rb4[16 + (col >> 2)];
+            const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
+            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dp[h][c]) - d4.x);
+            const float d1 = __uint_as_float(pa & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 1]) - d4.y);
+            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dp[h][c + 2]) - d4.z);
+            const float d3 = __uint_as_float(pb & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 3]) - d4.w);
             dsk[col >> 1] = pack_bf16x2(d0, d1);
+            dsk[(col >> 1) + 1] = pack_bf16x2(d2, d3);
           }
         }
-        tmem_st32(t_dp, dsk);  // over dP^T columns this warpgroup has read
+        tmem_st32(t_dp, pk);        // P^T over dP^T columns this warpgroup has read
+        tmem_st32(t_dp + 32, dsk);  // dS^T next to it
       }
       tmem_st_wait();
       tc_fence_before();
@@ -339,7 +398,7 @@ struct DqCfg {
 struct DqBarriers {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], dp_full, ds_ready, mma_done, teardown;
+  uint64_t s_full[2], dp_full, dp_free, ds_ready, mma_done, teardown;
   uint32_t tmem_base;
   int abort;
 };
@@ -374,6 +433,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(&bars.s_full[0], 1);
     mbar_init(&bars.s_full[1], 1);
     mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.teardown, 1);
@@ -427,17 +487,25 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dQ: dS from TMEM, K MN-major
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
+      uint64_t dq_[D / 16], ddo_[D / 16], dk_[D / 16], dv_[D / 16], dkm[C::BK / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
+        ddo_[kk] = sdesc_sw128(do_base + off, 16, 1024);
+        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
+        dv_[kk] = sdesc_sw128(v_base + off, 16, 1024);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::BK / 16; ++kk) dkm[kk] = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
       auto issue_s = [&](int j) -> bool {
         const int sk = j % C::kKStages;
         if (!mbar_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ks = k_base + sk * C::kTileBytes;
+        const uint32_t ko = sk * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS + 128 * (j & 1), sdesc_sw128(q_base + off, 16, 1024),
-                 sdesc_sw128(ks + off, 16, 1024), kIdKK, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColS + 128 * (j & 1), dq_[kk], desc_add(dk_[kk], ko), kIdKK, kk > 0);
         mma_commit(&bars.s_full[j & 1]);
         return true;
       };
@@ -445,32 +513,32 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         const int sv = j % C::kVStages;
         if (!mbar_wait(&bars.v_full[sv], (j / C::kVStages) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vs = v_base + sv * C::kTileBytes;
+        const uint32_t vo = sv * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(do_base + off, 16, 1024), sdesc_sw128(vs + off, 16, 1024), kIdKK,
-                 kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColDP, ddo_[kk], desc_add(dv_[kk], vo), kIdKK, kk > 0);
         mma_commit(&bars.dp_full);
         mma_commit(&bars.v_empty[sv]);
         return true;
       };
-      // S for block j+2 goes into the buffer that held dS of block j; dP of
-      // block j+1 overwrites dP of block j. Both follow the dQ product of
-      // block j in issue order, which reads that dS first.
+      // dP of block j+1 is issued as soon as both warpgroups have read dP of
+      // block j, so it overlaps their dS work. S of block j+2 goes into the
+      // buffer that held dS of block j, after the dQ product of block j in
+      // issue order (the products of one thread execute in that order).
       bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
       ok = ok && issue_s(0) && issue_dp(0) && (nk < 2 || issue_s(1));
       for (int j = 0; ok && j < nk; ++j) {
+        if (j + 1 < nk) {
+          if (!(ok = mbar_wait(&bars.dp_free, j & 1, abort_flag))) break;
+          if (!(ok = issue_dp(j + 1))) break;
+        }
         if (!(ok = mbar_wait(&bars.ds_ready, j & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t ks = k_base + (j % C::kKStages) * C::kTileBytes;
+        const uint32_t ko = (j % C::kKStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * (j & 1) + packed_col(kk),
-                 sdesc_sw128(ks + kk * 2048, kPanelBytes, 1024), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * (j & 1) + packed_col(kk), desc_add(dkm[kk], ko), kIdTS,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.k_empty[j % C::kKStages]);
-        if (j + 1 < nk && !(ok = issue_dp(j + 1))) break;
         if (j + 2 < nk && !(ok = issue_s(j + 2))) break;
       }
       mma_commit(&bars.mma_done);
@@ -520,18 +588,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      uint32_t dsk[32];
+      uint32_t dp[2][32], dsk[32];
+      tmem_ld32(tmem + lane_off + C::kColDP + 64 * w, dp[0]);
+      tmem_ld32(tmem + lane_off + C::kColDP + 64 * w + 32, dp[1]);
+      tmem_ld_wait(dp[0]);
+      tmem_ld_wait(dp[1]);
+      tc_fence_before();
+      mbar_arrive(&bars.dp_free);  // dP is in registers: the next block's dP may overwrite it
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + C::kColDP + 64 * w + 32 * h, dp);
-        tmem_ld_wait(dp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int col = 32 * h + c;
           const uint32_t pp = pk[col >> 1];
-          const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(dp[c]) - dsum);
-          const float d1 = __uint_as_float(pp & 0xFFFF0000u) * (__uint_as_float(dp[c + 1]) - dsum);
+          const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(dp[h][c]) - dsum);
+          const float d1 = __uint_as_float(pp & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 1]) - dsum);
           dsk[col >> 1] = pack_bf16x2(d0, d1);
         }
       }

@@ -153,14 +153,22 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       const uint32_t k_base = smem_u32(smem + C::kOffK);
       const uint32_t v_base = smem_u32(smem + C::kOffV);
+      // Descriptors for Q tile 0 and K/V stage 0; other tiles and stages add a byte offset
+      // to the start-address field (bits [0,14) hold address >> 4).
+      uint64_t dq_[D / 16], dk_[D / 16], dvm[C::BN / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
+        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
+        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk) dvm[kk] = sdesc_sw128(v_base + kk * 2048, C::kPanelBytes, 1024);
       auto issue_s = [&](int t, int st) {
         const uint32_t d_s = tmem + C::col_s(t);
+        const uint32_t qo = (uint32_t)(t * C::kTileBytes) >> 4, ko = (uint32_t)(st * C::kTileBytes) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
-          mma_ss(d_s, sdesc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
-                 sdesc_sw128(k_base + st * C::kTileBytes + off, 16, 1024), kIdS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(d_s, dq_[kk] + qo, dk_[kk] + ko, kIdS, kk > 0);
         mma_commit(&bars.s_full[t]);
       };
       bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.k_full[0], 0, abort_flag);
@@ -187,10 +195,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             tc_fence_after();
             const uint32_t a_p = tmem + C::col_s(t);
             const uint32_t d_o = tmem + C::col_o(t);
+            const uint32_t vo = (uint32_t)(s * C::kTileBytes) >> 4;
 #pragma unroll
             for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, sdesc_sw128(v_base + s * C::kTileBytes + kk * 2048, C::kPanelBytes, 1024),
-                     kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(d_o, a_p + kk * 8, dvm[kk] + vo, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars.o_done[t]);
           }
           if (jn < nb[t]) {

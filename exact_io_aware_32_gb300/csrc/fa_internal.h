@@ -19,6 +19,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (loads)
+  CUtensorMap tm_q64, tm_do64;          // bf16 [BH][N][d], box 64 x 64 x 1, 128B swizzle (loads)
   CUtensorMap tm_dq, tm_dk, tm_dv;      // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
   const void* o;                        // bf16 [BH][N][d]
   const void* dO;                       // bf16 [BH][N][d]
