@@ -29,6 +29,8 @@
 // next product. Each S or dP tile is released to the MMA warp as soon as the
 // warpgroups hold it in registers, so the next tile's product overlaps their
 // elementwise work.
+#include <cuda_bf16.h>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -190,28 +192,19 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV, dK: A from TMEM, B MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
-      // Descriptors for stage 0; stage 1 adds kTileBytes.
-      uint64_t dk_[D / 16], dv_[D / 16], dq_[D / 16], ddo_[D / 16], dqm[C::BQ / 16], ddom[C::BQ / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
-        dv_[kk] = sdesc_sw128(v_base + off, 16, 1024);
-        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
-        ddo_[kk] = sdesc_sw128(do_base + off, 16, 1024);
-      }
-#pragma unroll
-      for (int kk = 0; kk < C::BQ / 16; ++kk) {
-        dqm[kk] = sdesc_sw128(q_base + kk * 2048, kPanelBytes, 1024);
-        ddom[kk] = sdesc_sw128(do_base + kk * 2048, kPanelBytes, 1024);
-      }
+      // Descriptors of stage 0; k-steps and stage 1 add a byte offset / 16 to the
+      // start-address field (bits [0,14)).
+      const uint64_t dk0 = sdesc_sw128(k_base, 16, 1024), dv0 = sdesc_sw128(v_base, 16, 1024);
+      const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), ddo0 = sdesc_sw128(do_base, 16, 1024);
+      const uint64_t dqm0 = sdesc_sw128(q_base, kPanelBytes, 1024), ddom0 = sdesc_sw128(do_base, kPanelBytes, 1024);
+      auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int it) -> bool {  // S^T = K Q_i^T
         const int s = it & 1;
         if (!mbar_wait(&bars.qd_full[s], (it >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColS, dk_[kk], desc_add(dq_[kk], so), kIdKK, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
         mma_commit(&bars.s_full);
         return true;
       };
@@ -219,7 +212,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         const uint32_t so = (it & 1) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, dv_[kk], desc_add(ddo_[kk], so), kIdKK, kk > 0);
+          mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
         mma_commit(&bars.dp_full);
       };
       // S^T of block i+1 is issued as soon as both warpgroups have read S^T of
@@ -240,11 +233,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), desc_add(ddom[kk], so), kIdTS,
+          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + so) >> 4), kIdTS,
                  (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), desc_add(dqm[kk], so), kIdTS,
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + so) >> 4), kIdTS,
                  (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.qd_empty[s]);
         if (it + 1 < n_iter) issue_dp(it + 1);
@@ -264,12 +257,12 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;  // dP^T, then P^T | dS^T (bf16)
     const float sl2 = a.scale_log2;
     const bool key_ok = key < N;
-    // Threads 0-63 of the warpgroup fetch lse (log2 units) of the group's 64
-    // queries, threads 64-127 fetch D; one block ahead, through registers.
+    // Threads 0-63 of the warpgroup fetch -lse (log2 units) of the group's 64
+    // queries, threads 64-127 fetch -D; one block ahead, through registers.
     auto fetch = [&](int it) -> float {
       const int q = (i_start + it) * C::BQ + 64 * w + (tt & 63);
-      if (tt < 64) return q < N ? a.lse[(size_t)bh * N + q] * kLog2e : INFINITY;  // 2^(x - inf) = 0 past N
-      return q < N ? a.Dsum[(size_t)bh * N + q] : 0.f;
+      if (tt < 64) return q < N ? -a.lse[(size_t)bh * N + q] * kLog2e : -INFINITY;  // 2^(x - inf) = 0 past N
+      return q < N ? -a.Dsum[(size_t)bh * N + q] : 0.f;
     };
     float next = n_iter > 0 ? fetch(0) : 0.f;
     bool ok = true;
@@ -297,20 +290,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
         // causal: query q0 + 64 w + col sees key kblk * BK + r only if q0 + 64 w + col >= key
         const int lim = CAUSAL ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
+        const float2 scale2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const int col = 32 * h + c;  // within the group's 64 queries
-            const float4 l4 = rb4[col >> 2];
-            float p0 = ex2(fmaf(__uint_as_float(sr[h][c]), sl2, -l4.x));
-            float p1 = ex2(fmaf(__uint_as_float(sr[h][c + 1]), sl2, -l4.y));
-            float p2 = ex2(fmaf(__uint_as_float(sr[h][c + 2]), sl2, -l4.z));
-            float p3 = ex2(fmaf(__uint_as_float(sr[h][c + 3]), sl2, -l4.w));
-            if (col < lim || !key_ok) p0 = 0.f;
-            if (col + 1 < lim || !key_ok) p1 = 0.f;
-            if (col + 2 < lim || !key_ok) p2 = 0.f;
-            if (col + 3 < lim || !key_ok) p3 = 0.f;
+            const float4 nl = rb4[col >> 2];  // -lse
+            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2,
+                                     make_float2(nl.x, nl.y));
+            const float2 x23 = ffma2(make_float2(__uint_as_float(sr[h][c + 2]), __uint_as_float(sr[h][c + 3])),
+                                     scale2, make_float2(nl.z, nl.w));
+            const float p0 = (col >= lim && key_ok) ? ex2(x01.x) : 0.f;
+            const float p1 = (col + 1 >= lim && key_ok) ? ex2(x01.y) : 0.f;
+            const float p2 = (col + 2 >= lim && key_ok) ? ex2(x23.x) : 0.f;
+            const float p3 = (col + 3 >= lim && key_ok) ? ex2(x23.y) : 0.f;
             pk[col >> 1] = pack_bf16x2(p0, p1);
             pk[(col >> 1) + 1] = pack_bf16x2(p2, p3);
           }
@@ -323,24 +317,25 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       }
       tc_fence_after();
       {
-        uint32_t dp[2][32], dsk[32];
-        tmem_ld32(t_dp, dp[0]);
-        tmem_ld32(t_dp + 32, dp[1]);
-        tmem_ld_wait(dp[0]);
-        tmem_ld_wait(dp[1]);
+        uint32_t dsk[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          uint32_t dp[32];
+          tmem_ld32(t_dp + 32 * h, dp);
+          tmem_ld_wait(dp);
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const int col = 32 * h + c;
-            const float4 d4 = rb4[16 + (col >> 2)];
+            const float4 nd = rb4[16 + (col >> 2)];  // -D
             const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
-            const float d0 = __uint_as_float(pa << 16) * (__uint_as_float(dp[h][c]) - d4.x);
-            const float d1 = __uint_as_float(pa & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 1]) - d4.y);
-            const float d2 = __uint_as_float(pb << 16) * (__uint_as_float(dp[h][c + 2]) - d4.z);
-            const float d3 = __uint_as_float(pb & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 3]) - d4.w);
-            dsk[col >> 1] = pack_bf16x2(d0, d1);
-            dsk[(col >> 1) + 1] = pack_bf16x2(d2, d3);
+            const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
+                                     fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                           make_float2(nd.x, nd.y)));
+            const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
+                                     fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                                           make_float2(nd.z, nd.w)));
+            dsk[col >> 1] = pack_bf16x2(d01.x, d01.y);
+            dsk[(col >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
           }
         }
         tmem_st32(t_dp, pk);        // P^T over dP^T columns this warpgroup has read
@@ -487,17 +482,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dQ: dS from TMEM, K MN-major
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
-      uint64_t dq_[D / 16], ddo_[D / 16], dk_[D / 16], dv_[D / 16], dkm[C::BK / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
-        ddo_[kk] = sdesc_sw128(do_base + off, 16, 1024);
-        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
-        dv_[kk] = sdesc_sw128(v_base + off, 16, 1024);
-      }
-#pragma unroll
-      for (int kk = 0; kk < C::BK / 16; ++kk) dkm[kk] = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
+      const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), ddo0 = sdesc_sw128(do_base, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(k_base, 16, 1024), dv0 = sdesc_sw128(v_base, 16, 1024);
+      const uint64_t dkm0 = sdesc_sw128(k_base, kPanelBytes, 1024);
+      auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int j) -> bool {
         const int sk = j % C::kKStages;
         if (!mbar_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
@@ -505,7 +493,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         const uint32_t ko = sk * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + 128 * (j & 1), dq_[kk], desc_add(dk_[kk], ko), kIdKK, kk > 0);
+          mma_ss(tmem + C::kColS + 128 * (j & 1), dq0 + koff(kk), dk0 + koff(kk) + (ko >> 4), kIdKK, kk > 0);
         mma_commit(&bars.s_full[j & 1]);
         return true;
       };
@@ -515,7 +503,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         tc_fence_after();
         const uint32_t vo = sv * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColDP, ddo_[kk], desc_add(dv_[kk], vo), kIdKK, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + (vo >> 4), kIdKK, kk > 0);
         mma_commit(&bars.dp_full);
         mma_commit(&bars.v_empty[sv]);
         return true;
@@ -536,7 +525,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         const uint32_t ko = (j % C::kKStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * (j & 1) + packed_col(kk), desc_add(dkm[kk], ko), kIdTS,
+          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * (j & 1) + packed_col(kk), dkm0 + ((kk * 2048 + ko) >> 4), kIdTS,
                  (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.k_empty[j % C::kKStages]);
         if (j + 2 < nk && !(ok = issue_s(j + 2))) break;
@@ -566,7 +555,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       const int k0 = j * C::BK + 64 * w;  // first key of this warpgroup's columns
       // keys past the causal diagonal or past N get P = 0; keep key k0 + col iff col <= lim
       const int lim = CAUSAL ? min(q, N - 1) - k0 : N - 1 - k0;
-      uint32_t pk[32];
+      float pf[64];
+      const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t sr[32];
@@ -575,11 +565,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int col = 32 * h + c;
-          float p0 = ex2(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
-          if (col > lim) p0 = 0.f;
-          if (col + 1 > lim) p1 = 0.f;
-          pk[col >> 1] = pack_bf16x2(p0, p1);
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, shift2);
+          pf[col] = col <= lim ? ex2(x.x) : 0.f;
+          pf[col + 1] = col + 1 <= lim ? ex2(x.y) : 0.f;
         }
       }
       ok = mbar_wait(&bars.dp_full, j & 1, abort_flag);
@@ -595,15 +583,17 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       tmem_ld_wait(dp[1]);
       tc_fence_before();
       mbar_arrive(&bars.dp_free);  // dP is in registers: the next block's dP may overwrite it
+      const float2 nd2 = make_float2(-dsum, -dsum);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int col = 32 * h + c;
-          const uint32_t pp = pk[col >> 1];
-          const float d0 = __uint_as_float(pp << 16) * (__uint_as_float(dp[h][c]) - dsum);
-          const float d1 = __uint_as_float(pp & 0xFFFF0000u) * (__uint_as_float(dp[h][c + 1]) - dsum);
-          dsk[col >> 1] = pack_bf16x2(d0, d1);
+          // dS = P (dP - D), with P rounded to bf16 as the other products see it
+          const float2 pb = make_float2(__bfloat162float(__float2bfloat16_rn(pf[col])),
+                                        __bfloat162float(__float2bfloat16_rn(pf[col + 1])));
+          const float2 d = fmul2(pb, fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
+          dsk[col >> 1] = pack_bf16x2(d.x, d.y);
         }
       }
       tmem_st32(t_s, dsk);  // over S columns this warpgroup has read

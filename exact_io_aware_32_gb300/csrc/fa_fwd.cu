@@ -153,22 +153,18 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       const uint32_t k_base = smem_u32(smem + C::kOffK);
       const uint32_t v_base = smem_u32(smem + C::kOffV);
-      // Descriptors for Q tile 0 and K/V stage 0; other tiles and stages add a byte offset
-      // to the start-address field (bits [0,14) hold address >> 4).
-      uint64_t dq_[D / 16], dk_[D / 16], dvm[C::BN / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
-        dq_[kk] = sdesc_sw128(q_base + off, 16, 1024);
-        dk_[kk] = sdesc_sw128(k_base + off, 16, 1024);
-      }
-#pragma unroll
-      for (int kk = 0; kk < C::BN / 16; ++kk) dvm[kk] = sdesc_sw128(v_base + kk * 2048, C::kPanelBytes, 1024);
+      // Descriptors of Q tile 0 and K/V stage 0. Other k-steps, tiles and stages
+      // add a byte offset / 16 to the start-address field (bits [0,14)).
+      const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), dk0 = sdesc_sw128(k_base, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(v_base, C::kPanelBytes, 1024);
       auto issue_s = [&](int t, int st) {
         const uint32_t d_s = tmem + C::col_s(t);
         const uint32_t qo = (uint32_t)(t * C::kTileBytes) >> 4, ko = (uint32_t)(st * C::kTileBytes) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(d_s, dq_[kk] + qo, dk_[kk] + ko, kIdS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d_s, dq0 + qo + off, dk0 + ko + off, kIdS, kk > 0);
+        }
         mma_commit(&bars.s_full[t]);
       };
       bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.k_full[0], 0, abort_flag);
@@ -198,7 +194,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             const uint32_t vo = (uint32_t)(s * C::kTileBytes) >> 4;
 #pragma unroll
             for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, dvm[kk] + vo, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * (2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars.o_done[t]);
           }
           if (jn < nb[t]) {
@@ -250,9 +246,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      for (int c = 0; c < 128; c += 4) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]));
+      }
+      const float mx = fmaxf(mx0, mx1);
       const float m_new = fmaxf(m_ref, mx * sl2);
       float alpha = 1.f;
       const bool move = m_new > m_ref + kRescaleThreshold;
@@ -261,19 +261,23 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         m_ref = m_new;
       }
       const bool rescale = __any_sync(0xffffffffu, move && j > 0);
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[2][32];
+      float2 sum = make_float2(0.f, 0.f);
+      const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_ref, -m_ref);
+      // P as bf16 pairs over the first 64 columns of S_t (all of S_t is already in
+      // registers), 32 scores at a time.
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -m_ref));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), sl2, -m_ref));
-        sum0 += p0;
-        sum1 += p1;
-        pk[c >> 6][(c & 63) >> 1] = pack_bf16x2(p0, p1);
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), scale2, shift2);
+          const float2 p = make_float2(ex2(x.x), ex2(x.y));
+          sum = fadd2(sum, p);
+          pk[c >> 1] = pack_bf16x2(p.x, p.y);
+        }
+        tmem_st16(t_s + 16 * ch, pk);
       }
-      l_sum = l_sum * alpha + (sum0 + sum1);
-      tmem_st32(t_s, pk[0]);
-      tmem_st32(t_s + 32, pk[1]);
+      l_sum = l_sum * alpha + (sum.x + sum.y);
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
