@@ -194,7 +194,7 @@ def cpu_baseline(w, causal: bool, budget_s: float = 12.0) -> dict:
 
 # ---------------------------------------------------------------------- GPU arm
 def kernel_traffic(source: str, kernel: str):
-    """DRAM bytes per launch from a committed ncu capture, or None if the kernel changed since."""
+    """DRAM bytes per call from a committed ncu capture, or None if the kernel source changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -337,7 +337,7 @@ def run_gpu(args, w, causal: bool):
     burst = peaks["bf16_tflops"]
     sustained = peaks.get("bf16_tflops_sustained", burst)
     achieved = f_bwd / bwd_s / 1e12
-    traffic = kernel_traffic("fa_bwd.cu", f"fa_bwd_main_kernel<{d},{str(causal).lower()}>")
+    traffic = kernel_traffic("fa_bwd.cu", f"fa_bwd<{d},{str(causal).lower()}>")
     result = {
         "metric": METRIC,
         "value": round(value / 1e12, 2),
@@ -367,7 +367,7 @@ def run_gpu(args, w, causal: bool):
         "pct_of_peak": round(100 * value / 1e12 / world / burst, 2),
         "peak_basis": f"{peaks['source']} dense bf16 burst {burst} TFLOP/s per GPU",
         "roofline": {
-            "kernel": "fa_bwd (prep + main + dq cast; main dominates)",
+            "kernel": "fa_bwd call: D prep + dK/dV kernel + dQ kernel (shares in profiles/)",
             "bound": "tensor", "achieved": round(achieved, 2), "peak": sustained, "unit": "TFLOP/s",
             "frac": round(achieved / sustained, 4), "traffic": traffic,
             "peak_basis": f"{peaks['source']} sustained dense bf16 (kernel timed inside a long step)",

@@ -84,13 +84,20 @@ struct DkdvCfg {
   static constexpr int BK = 128;  // keys per CTA
   static constexpr int BQ = 128;  // queries per iteration
   static constexpr int kTileBytes = (D / 64) * kPanelBytes;
+  // Q is needed first in each block (by S^T) and dO later (by dP^T and dV), so
+  // Q gets the deeper ring: its load for block i+2 starts when dK of block i-1
+  // completes.
+  static constexpr int kQStages = D == 128 ? 3 : 4;
+  static constexpr int kDOStages = D == 128 ? 2 : 4;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
-  static constexpr int kOffQ = 2 * kTileBytes;   // 2 stages
-  static constexpr int kOffDO = 4 * kTileBytes;  // 2 stages
-  static constexpr int kOffRow = 6 * kTileBytes;  // [parity][warpgroup][lse(64) | D(64)] fp32
+  static constexpr int kOffQ = 2 * kTileBytes;
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffRow = kOffDO + kDOStages * kTileBytes;  // [parity][warpgroup][-lse(64) | -D(64)] fp32
   static constexpr int kOffBar = kOffRow + 2 * 2 * 128 * 4;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  // No alignment slack: the kernel checks that dynamic shared memory starts on
+  // a 1024-byte boundary (the 128-byte swizzle atoms need it).
+  static constexpr int kSmemBytes = kOffBar + 256;
   static constexpr uint32_t kColS = 0;     // S^T fp32
   static constexpr uint32_t kColDP = 128;  // dP^T fp32; warpgroup w then writes P^T (bf16) over its
                                            // columns [128 + 64 w, +32) and dS^T over [+32, +64)
@@ -100,7 +107,7 @@ struct DkdvCfg {
 
 struct DkdvBarriers {
   uint64_t kv_full;
-  uint64_t qd_full[2], qd_empty[2];
+  uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
   uint64_t s_full, s_free, dp_full, ds_ready, mma_done, teardown;
   uint32_t tmem_base;
   int abort;
@@ -121,7 +128,11 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {  // uniform over the CTA: every thread leaves before any barrier
+    if (threadIdx.x == 0) atomicOr(a.status, 16u);
+    return;
+  }
   DkdvBarriers& bars = *reinterpret_cast<DkdvBarriers*>(smem + C::kOffBar);
   volatile int* abort_flag = &bars.abort;
   float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow);
@@ -137,9 +148,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.qd_full[s], 1);
-      mbar_init(&bars.qd_empty[s], 1);
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+    }
+    for (int s = 0; s < C::kDOStages; ++s) {
+      mbar_init(&bars.do_full[s], 1);
+      mbar_init(&bars.do_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.s_free, 256);
@@ -160,9 +175,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    // Lane 0 loads K and V, then runs the Q ring; lane 1 runs the dO ring.
     if (lane == 0) {
       tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_do);
       mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
       for (int pn = 0; pn < D / 64; ++pn) {
         tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.kv_full, pn * 64, kblk * C::BK, bh);
@@ -170,20 +185,31 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       }
       int issued = 0;
       for (int it = 0; it < n_iter; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(&bars.qd_empty[s], ((it >> 1) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars.qd_full[s], 2 * C::kTileBytes);
-        const int q0 = (i_start + it) * C::BQ;
-        for (int pn = 0; pn < D / 64; ++pn) {
-          tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.qd_full[s], pn * 64,
-                      q0, bh);
-          tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.qd_full[s], pn * 64,
-                      q0, bh);
-        }
+        const int s = it % C::kQStages;
+        if (!mbar_wait(&bars.q_empty[s], ((it / C::kQStages) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.q_full[s], C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.q_full[s], pn * 64,
+                      (i_start + it) * C::BQ, bh);
         issued = it + 1;
       }
       mbar_wait_drain(&bars.kv_full, 0);
-      for (int i = max(0, issued - 2); i < issued; ++i) mbar_wait_drain(&bars.qd_full[i & 1], (i >> 1) & 1);
+      for (int i = max(0, issued - C::kQStages); i < issued; ++i)
+        mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
+    } else if (lane == 1) {
+      tma_prefetch_desc(&a.tm_do);
+      int issued = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it % C::kDOStages;
+        if (!mbar_wait(&bars.do_empty[s], ((it / C::kDOStages) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.do_full[s], C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.do_full[s], pn * 64,
+                      (i_start + it) * C::BQ, bh);
+        issued = it + 1;
+      }
+      for (int i = max(0, issued - C::kDOStages); i < issued; ++i)
+        mbar_wait_drain(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -199,8 +225,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       const uint64_t dqm0 = sdesc_sw128(q_base, kPanelBytes, 1024), ddom0 = sdesc_sw128(do_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int it) -> bool {  // S^T = K Q_i^T
-        const int s = it & 1;
-        if (!mbar_wait(&bars.qd_full[s], (it >> 1) & 1, abort_flag)) return false;
+        const int s = it % C::kQStages;
+        if (!mbar_wait(&bars.q_full[s], (it / C::kQStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
 #pragma unroll
@@ -208,23 +234,26 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         mma_commit(&bars.s_full);
         return true;
       };
-      auto issue_dp = [&](int it) {  // dP^T = V dO_i^T (dO_i is in the stage S^T of block i waited for)
-        const uint32_t so = (it & 1) * C::kTileBytes;
+      auto issue_dp = [&](int it) -> bool {  // dP^T = V dO_i^T
+        const int s = it % C::kDOStages;
+        if (!mbar_wait(&bars.do_full[s], (it / C::kDOStages) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t so = s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
         mma_commit(&bars.dp_full);
+        return true;
       };
       // S^T of block i+1 is issued as soon as both warpgroups have read S^T of
       // block i, so it overlaps their elementwise work. dP^T of block i+1
       // follows dV and dK of block i in issue order: the products of one
       // thread execute in that order, so dV and dK have read P^T and dS^T
       // before dP^T overwrites the columns that hold them.
-      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag) && issue_s(0);
-      if (ok) issue_dp(0);
+      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag) && issue_s(0) && issue_dp(0);
       for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it & 1;
-        const uint32_t so = s * C::kTileBytes;
+        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
         if (it + 1 < n_iter) {
           if (!(ok = mbar_wait(&bars.s_free, it & 1, abort_flag))) break;
           if (!(ok = issue_s(it + 1))) break;
@@ -233,14 +262,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + so) >> 4), kIdTS,
+          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4), kIdTS,
                  (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.do_empty[ds]);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + so) >> 4), kIdTS,
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4), kIdTS,
                  (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.qd_empty[s]);
-        if (it + 1 < n_iter) issue_dp(it + 1);
+        mma_commit(&bars.q_empty[qs]);
+        if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
       }
       mma_commit(&bars.mma_done);
       mma_commit(&bars.teardown);
@@ -372,6 +402,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 }
 
 // ============================================================================ dQ
+// One CTA per 128-row query block (TMEM lane = query), 128 keys per
+// iteration. Q is the same for every key block, so after loading it once the
+// warpgroups copy it into TMEM and S = Q K^T reads its A operand from there.
+// dS has TMEM columns of its own, so S, dP and dQ of consecutive key blocks
+// only wait for the warpgroups to have read the previous tile.
 template <int D>
 struct DqCfg {
   static constexpr int BQ = 128;  // queries per CTA
@@ -385,18 +420,39 @@ struct DqCfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;
-  static constexpr uint32_t kColS = 0;     // two S buffers of 128 fp32 columns; dS bf16 reuses them
-  static constexpr uint32_t kColDP = 256;  // dP fp32
-  static constexpr uint32_t kColDQ = 384;  // dQ accumulator, D columns
+  static constexpr uint32_t kColQ = 0;            // Q, bf16 pairs, D / 2 columns
+  static constexpr uint32_t kColDS = D / 2;       // dS, bf16 pairs, 64 columns (warpgroup w: [32 w, 32 w + 32))
+  static constexpr uint32_t kColS = D / 2 + 64;   // S fp32, 128 columns
+  static constexpr uint32_t kColDP = D / 2 + 192;  // dP fp32, 128 columns
+  static constexpr uint32_t kColDQ = D / 2 + 320;  // dQ accumulator, D columns
 };
 
 struct DqBarriers {
-  uint64_t q_full;
+  uint64_t q_full, qt_ready;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], dp_full, dp_free, ds_ready, mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_done, mma_done, teardown;
   uint32_t tmem_base;
   int abort;
 };
+
+// Copies row r (D bf16) of a 128-row, 128-byte-swizzled tile into TMEM as D / 2
+// columns of bf16 pairs at taddr (this thread's lane).
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    uint32_t v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 x = *reinterpret_cast<const uint4*>(tile + h * kPanelBytes + r * 128 + ((k ^ (r & 7)) << 4));
+      v[4 * k] = x.x;
+      v[4 * k + 1] = x.y;
+      v[4 * k + 2] = x.z;
+      v[4 * k + 3] = x.w;
+    }
+    tmem_st32(taddr + 32 * h, v);
+  }
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
@@ -417,6 +473,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.qt_ready, 256);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -425,11 +482,12 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
-    mbar_init(&bars.s_full[0], 1);
-    mbar_init(&bars.s_full[1], 1);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.ds_ready, 256);
+    mbar_init(&bars.dq_done, 1);
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
@@ -478,57 +536,56 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S, dP: both operands K-major
+      constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S (A from TMEM), dP: B K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dQ: dS from TMEM, K MN-major
-      const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
-      const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), ddo0 = sdesc_sw128(do_base, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(k_base, 16, 1024), dv0 = sdesc_sw128(v_base, 16, 1024);
+      const uint64_t ddo0 = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
       const uint64_t dkm0 = sdesc_sw128(k_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
         const int sk = j % C::kKStages;
         if (!mbar_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t ko = sk * C::kTileBytes;
+        const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + 128 * (j & 1), dq0 + koff(kk), dk0 + koff(kk) + (ko >> 4), kIdKK, kk > 0);
-        mma_commit(&bars.s_full[j & 1]);
+          mma_ts(tmem + C::kColS, tmem + C::kColQ + 8 * kk, dk0 + koff(kk) + ko, kIdKK, kk > 0);
+        mma_commit(&bars.s_full);
         return true;
       };
-      auto issue_dp = [&](int j) -> bool {
+      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T
         const int sv = j % C::kVStages;
         if (!mbar_wait(&bars.v_full[sv], (j / C::kVStages) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vo = sv * C::kTileBytes;
+        const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + (vo >> 4), kIdKK, kk > 0);
+          mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
         mma_commit(&bars.dp_full);
         mma_commit(&bars.v_empty[sv]);
         return true;
       };
-      // dP of block j+1 is issued as soon as both warpgroups have read dP of
-      // block j, so it overlaps their dS work. S of block j+2 goes into the
-      // buffer that held dS of block j, after the dQ product of block j in
-      // issue order (the products of one thread execute in that order).
-      bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
-      ok = ok && issue_s(0) && issue_dp(0) && (nk < 2 || issue_s(1));
+      // S and dP of block j+1 are issued once the warpgroups have read those of
+      // block j; dQ of block j once they have written dS of block j.
+      bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.qt_ready, 0, abort_flag) &&
+                issue_s(0) && issue_dp(0);
       for (int j = 0; ok && j < nk; ++j) {
         if (j + 1 < nk) {
+          if (!(ok = mbar_wait(&bars.s_free, j & 1, abort_flag))) break;
+          if (!(ok = issue_s(j + 1))) break;
           if (!(ok = mbar_wait(&bars.dp_free, j & 1, abort_flag))) break;
           if (!(ok = issue_dp(j + 1))) break;
         }
         if (!(ok = mbar_wait(&bars.ds_ready, j & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t ko = (j % C::kKStages) * C::kTileBytes;
+        const uint32_t ko = (uint32_t)((j % C::kKStages) * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * (j & 1) + packed_col(kk), dkm0 + ((kk * 2048 + ko) >> 4), kIdTS,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
+                 dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.dq_done);
         mma_commit(&bars.k_empty[j % C::kKStages]);
-        if (j + 2 < nk && !(ok = issue_s(j + 2))) break;
       }
       mma_commit(&bars.mma_done);
       mma_commit(&bars.teardown);
@@ -543,10 +600,20 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     const float sl2 = a.scale_log2;
     const float lse2 = q < N ? a.lse[(size_t)bh * N + q] * kLog2e : INFINITY;  // rows past N: P = 0
     const float dsum = q < N ? a.Dsum[(size_t)bh * N + q] : 0.f;
-    bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      const uint32_t t_s = tmem + lane_off + C::kColS + 128 * (j & 1) + 64 * w;
-      ok = mbar_wait(&bars.s_full[j & 1], (j >> 1) & 1, abort_flag);
+    // Q into TMEM (row r = lane r): warpgroup w copies the 64-column panel w.
+    bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && w < D / 64) {
+      tile_row_to_tmem<64>(smem + C::kOffQ + w * kPanelBytes, r, tmem + lane_off + C::kColQ + 32 * w);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(&bars.qt_ready);
+    const uint32_t t_s = tmem + lane_off + C::kColS + 64 * w;
+    const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;
+    const uint32_t t_ds = tmem + lane_off + C::kColDS + 32 * w;
+    for (int j = 0; ok && j < nk; ++j) {
+      ok = mbar_wait(&bars.s_full, j & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -556,18 +623,24 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       // keys past the causal diagonal or past N get P = 0; keep key k0 + col iff col <= lim
       const int lim = CAUSAL ? min(q, N - 1) - k0 : N - 1 - k0;
       float pf[64];
-      const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
+      {
+        uint32_t sr[2][32];
+        tmem_ld32(t_s, sr[0]);
+        tmem_ld32(t_s + 32, sr[1]);
+        tmem_ld_wait(sr[0]);
+        tmem_ld_wait(sr[1]);
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
+        const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[32];
-        tmem_ld32(t_s + 32 * h, sr);
-        tmem_ld_wait(sr);
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int col = 32 * h + c;
-          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, shift2);
-          pf[col] = col <= lim ? ex2(x.x) : 0.f;
-          pf[col + 1] = col + 1 <= lim ? ex2(x.y) : 0.f;
+          for (int c = 0; c < 32; c += 2) {
+            const int col = 32 * h + c;
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2, shift2);
+            pf[col] = col <= lim ? ex2(x.x) : 0.f;
+            pf[col + 1] = col + 1 <= lim ? ex2(x.y) : 0.f;
+          }
         }
       }
       ok = mbar_wait(&bars.dp_full, j & 1, abort_flag);
@@ -577,8 +650,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       }
       tc_fence_after();
       uint32_t dp[2][32], dsk[32];
-      tmem_ld32(tmem + lane_off + C::kColDP + 64 * w, dp[0]);
-      tmem_ld32(tmem + lane_off + C::kColDP + 64 * w + 32, dp[1]);
+      tmem_ld32(t_dp, dp[0]);
+      tmem_ld32(t_dp + 32, dp[1]);
       tmem_ld_wait(dp[0]);
       tmem_ld_wait(dp[1]);
       tc_fence_before();
@@ -596,7 +669,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
           dsk[col >> 1] = pack_bf16x2(d.x, d.y);
         }
       }
-      tmem_st32(t_s, dsk);  // over S columns this warpgroup has read
+      if (j > 0) {  // the dQ product of the previous block has read its dS
+        ok = mbar_wait(&bars.dq_done, (j - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(t_ds, dsk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
@@ -604,7 +685,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     // Epilogue: dq = bf16(scale * dQ); warpgroup w converts features [D/2 w, D/2 w + D/2).
     if (ok && nk > 0) ok = mbar_wait(&bars.mma_done, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    uint8_t* stage = smem + C::kOffQ;  // Q is no longer read once the last S has completed
+    uint8_t* stage = smem + C::kOffQ;  // Q in shared memory is not read after the copy into TMEM
     if (ok && nk > 0) {
       tc_fence_after();
       stage_row_bf16<D / 2>(tmem + lane_off + C::kColDQ + (D / 2) * w, stage, r, (D / 2) * w, a.scale);
