@@ -151,8 +151,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.Dsum = static_cast<float*>(workspace);
   if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_q64, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
-      !encode_3d(&a.tm_do64, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 64) ||
       !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "block_order.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -139,9 +140,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
-  const int bh = blockIdx.x;
-  const int kblk = blockIdx.y;  // key block 0 has the most query blocks under the causal mask: it goes first
   const int nq = (N + C::BQ - 1) / C::BQ;
+  int bh, kblk;  // key block 0 has the most query blocks under the causal mask: it goes first
+  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, kblk);
   const int i_start = CAUSAL ? kblk : 0;  // BQ == BK: query block i sees key block j iff i >= j
   const int n_iter = nq - i_start;
 
@@ -175,45 +176,54 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 loads K and V, then runs the Q ring; lane 1 runs the dO ring.
-    if (lane == 0) {
+    // K and V once, then Q and dO of each query block in block order, Q
+    // first (S^T needs it before dP^T needs dO). At d = 128 this is also the
+    // order in which their ring slots come free: dK of block i - 3 releases
+    // Q's slot, then dV of block i - 2 releases dO's. The whole warp waits;
+    // one elected lane issues.
+    if (elect_one()) {
       tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_do);
       mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
       for (int pn = 0; pn < D / 64; ++pn) {
         tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.kv_full, pn * 64, kblk * C::BK, bh);
         tma_load_3d(smem + C::kOffV + pn * kPanelBytes, &a.tm_v, &bars.kv_full, pn * 64, kblk * C::BK, bh);
       }
-      int issued = 0;
-      for (int it = 0; it < n_iter; ++it) {
-        const int s = it % C::kQStages;
-        if (!mbar_wait(&bars.q_empty[s], ((it / C::kQStages) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars.q_full[s], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.q_full[s], pn * 64,
-                      (i_start + it) * C::BQ, bh);
-        issued = it + 1;
-      }
-      mbar_wait_drain(&bars.kv_full, 0);
-      for (int i = max(0, issued - C::kQStages); i < issued; ++i)
-        mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
-    } else if (lane == 1) {
-      tma_prefetch_desc(&a.tm_do);
-      int issued = 0;
-      for (int it = 0; it < n_iter; ++it) {
-        const int s = it % C::kDOStages;
-        if (!mbar_wait(&bars.do_empty[s], ((it / C::kDOStages) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars.do_full[s], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.do_full[s], pn * 64,
-                      (i_start + it) * C::BQ, bh);
-        issued = it + 1;
-      }
-      for (int i = max(0, issued - C::kDOStages); i < issued; ++i)
-        mbar_wait_drain(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1);
     }
+    __syncwarp();
+    int q_issued = 0, do_issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int qs = it % C::kQStages, ds = it % C::kDOStages;
+      if (!warp_wait(&bars.q_empty[qs], ((it / C::kQStages) & 1) ^ 1, abort_flag)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffQ + qs * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.q_full[qs], pn * 64,
+                      (i_start + it) * C::BQ, bh);
+      }
+      __syncwarp();
+      q_issued = it + 1;
+      if (!warp_wait(&bars.do_empty[ds], ((it / C::kDOStages) & 1) ^ 1, abort_flag)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars.do_full[ds], C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffDO + ds * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.do_full[ds],
+                      pn * 64, (i_start + it) * C::BQ, bh);
+      }
+      __syncwarp();
+      do_issued = it + 1;
+    }
+    // let every copy still in flight land before the CTA can exit
+    mbar_wait_drain(&bars.kv_full, 0);
+    for (int i = max(0, q_issued - C::kQStages); i < q_issued; ++i)
+      mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
+    for (int i = max(0, do_issued - C::kDOStages); i < do_issued; ++i)
+      mbar_wait_drain(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp follows the schedule, so it stays converged and its
+    // operands warp-uniform; one elected lane issues each group of tcgen05 ops.
+    {
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV, dK: A from TMEM, B MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
@@ -226,23 +236,30 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int it) -> bool {  // S^T = K Q_i^T
         const int s = it % C::kQStages;
-        if (!mbar_wait(&bars.q_full[s], (it / C::kQStages) & 1, abort_flag)) return false;
+        if (!warp_wait(&bars.q_full[s], (it / C::kQStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
-        mma_commit(&bars.s_full);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
+          mma_commit(&bars.s_full);
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int it) -> bool {  // dP^T = V dO_i^T
         const int s = it % C::kDOStages;
-        if (!mbar_wait(&bars.do_full[s], (it / C::kDOStages) & 1, abort_flag)) return false;
+        if (!warp_wait(&bars.do_full[s], (it / C::kDOStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
-        mma_commit(&bars.dp_full);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
+          mma_commit(&bars.dp_full);
+        }
+        __syncwarp();
         return true;
       };
       // S^T of block i+1 is issued as soon as both warpgroups have read S^T of
@@ -250,30 +267,36 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       // follows dV and dK of block i in issue order: the products of one
       // thread execute in that order, so dV and dK have read P^T and dS^T
       // before dP^T overwrites the columns that hold them.
-      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag) && issue_s(0) && issue_dp(0);
+      bool ok = warp_wait(&bars.kv_full, 0, abort_flag) && issue_s(0) && issue_dp(0);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
         if (it + 1 < n_iter) {
-          if (!(ok = mbar_wait(&bars.s_free, it & 1, abort_flag))) break;
+          if (!(ok = warp_wait(&bars.s_free, it & 1, abort_flag))) break;
           if (!(ok = issue_s(it + 1))) break;
         }
-        if (!(ok = mbar_wait(&bars.ds_ready, it & 1, abort_flag))) break;
+        if (!(ok = warp_wait(&bars.ds_ready, it & 1, abort_flag))) break;
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-          mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4), kIdTS,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.do_empty[ds]);
+          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
+            mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
+                   kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.do_empty[ds]);
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4), kIdTS,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.q_empty[qs]);
+          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
+            mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
+                   kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.q_empty[qs]);
+        }
+        __syncwarp();
         if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
       }
-      mma_commit(&bars.mma_done);
-      mma_commit(&bars.teardown);
+      if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
+        mma_commit(&bars.mma_done);
+        mma_commit(&bars.teardown);
+      }
+      __syncwarp();
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
@@ -287,6 +310,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;  // dP^T, then P^T | dS^T (bf16)
     const float sl2 = a.scale_log2;
     const bool key_ok = key < N;
+    const bool keys_all_ok = (kblk + 1) * C::BK <= N;  // uniform over the CTA
     // Threads 0-63 of the warpgroup fetch -lse (log2 units) of the group's 64
     // queries, threads 64-127 fetch -D; one block ahead, through registers.
     auto fetch = [&](int it) -> float {
@@ -318,8 +342,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         tmem_ld_wait(sr[1]);
         tc_fence_before();
         mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
-        // causal: query q0 + 64 w + col sees key kblk * BK + r only if q0 + 64 w + col >= key
-        const int lim = CAUSAL ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
+        // Only the diagonal block (the first under the causal mask) and a ragged
+        // last key block need masking: there a hidden score becomes -inf, so P = 0
+        // (scale > 0). Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col >= key.
+        if ((CAUSAL && it == 0) || !keys_all_ok) {
+          const int lim = CAUSAL && it == 0 ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < lim || !key_ok) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
         const float2 scale2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -331,12 +362,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
                                      make_float2(nl.x, nl.y));
             const float2 x23 = ffma2(make_float2(__uint_as_float(sr[h][c + 2]), __uint_as_float(sr[h][c + 3])),
                                      scale2, make_float2(nl.z, nl.w));
-            const float p0 = (col >= lim && key_ok) ? ex2(x01.x) : 0.f;
-            const float p1 = (col + 1 >= lim && key_ok) ? ex2(x01.y) : 0.f;
-            const float p2 = (col + 2 >= lim && key_ok) ? ex2(x23.x) : 0.f;
-            const float p3 = (col + 3 >= lim && key_ok) ? ex2(x23.y) : 0.f;
-            pk[col >> 1] = pack_bf16x2(p0, p1);
-            pk[(col >> 1) + 1] = pack_bf16x2(p2, p3);
+            pk[col >> 1] = pack_bf16x2(ex2(x01.x), ex2(x01.y));
+            pk[(col >> 1) + 1] = pack_bf16x2(ex2(x23.x), ex2(x23.y));
           }
         }
       }
@@ -464,9 +491,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
-  const int bh = blockIdx.x;
   const int nq = (N + C::BQ - 1) / C::BQ;
-  const int qblk = CAUSAL ? (nq - 1 - (int)blockIdx.y) : (int)blockIdx.y;  // heaviest first when causal
+  int bh, blk;
+  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
+  const int qblk = CAUSAL ? nq - 1 - blk : blk;  // heaviest first under the causal mask
   const int nkv = (N + C::BK - 1) / C::BK;
   const int nk = CAUSAL ? min(qblk + 1, nkv) : nkv;  // key blocks this query block sees
 
@@ -535,7 +563,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Whole warp, converged; one elected lane issues (as in the dK/dV kernel).
+    {
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S (A from TMEM), dP: B K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dQ: dS from TMEM, K MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
@@ -545,50 +574,62 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
         const int sk = j % C::kKStages;
-        if (!mbar_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
+        if (!warp_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + C::kColS, tmem + C::kColQ + 8 * kk, dk0 + koff(kk) + ko, kIdKK, kk > 0);
-        mma_commit(&bars.s_full);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8 * kk, dk0 + koff(kk) + ko, kIdKK, kk > 0);
+          mma_commit(&bars.s_full);
+        }
+        __syncwarp();
         return true;
       };
       auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T
         const int sv = j % C::kVStages;
-        if (!mbar_wait(&bars.v_full[sv], (j / C::kVStages) & 1, abort_flag)) return false;
+        if (!warp_wait(&bars.v_full[sv], (j / C::kVStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
-        mma_commit(&bars.dp_full);
-        mma_commit(&bars.v_empty[sv]);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
+          mma_commit(&bars.dp_full);
+          mma_commit(&bars.v_empty[sv]);
+        }
+        __syncwarp();
         return true;
       };
       // S and dP of block j+1 are issued once the warpgroups have read those of
       // block j; dQ of block j once they have written dS of block j.
-      bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.qt_ready, 0, abort_flag) &&
+      bool ok = warp_wait(&bars.q_full, 0, abort_flag) && warp_wait(&bars.qt_ready, 0, abort_flag) &&
                 issue_s(0) && issue_dp(0);
       for (int j = 0; ok && j < nk; ++j) {
         if (j + 1 < nk) {
-          if (!(ok = mbar_wait(&bars.s_free, j & 1, abort_flag))) break;
+          if (!(ok = warp_wait(&bars.s_free, j & 1, abort_flag))) break;
           if (!(ok = issue_s(j + 1))) break;
-          if (!(ok = mbar_wait(&bars.dp_free, j & 1, abort_flag))) break;
+          if (!(ok = warp_wait(&bars.dp_free, j & 1, abort_flag))) break;
           if (!(ok = issue_dp(j + 1))) break;
         }
-        if (!(ok = mbar_wait(&bars.ds_ready, j & 1, abort_flag))) break;
+        if (!(ok = warp_wait(&bars.ds_ready, j & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t ko = (uint32_t)((j % C::kKStages) * C::kTileBytes);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
-                 dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.dq_done);
-        mma_commit(&bars.k_empty[j % C::kKStages]);
+          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
+            mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
+                   dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.dq_done);
+          mma_commit(&bars.k_empty[j % C::kKStages]);
+        }
+        __syncwarp();
       }
-      mma_commit(&bars.mma_done);
-      mma_commit(&bars.teardown);
+      if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
+        mma_commit(&bars.mma_done);
+        mma_commit(&bars.teardown);
+      }
+      __syncwarp();
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
@@ -620,9 +661,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       }
       tc_fence_after();
       const int k0 = j * C::BK + 64 * w;  // first key of this warpgroup's columns
-      // keys past the causal diagonal or past N get P = 0; keep key k0 + col iff col <= lim
-      const int lim = CAUSAL ? min(q, N - 1) - k0 : N - 1 - k0;
-      float pf[64];
+      uint32_t pk[32];  // P, this thread's row, keys k0 .. k0 + 63, as bf16 pairs
       {
         uint32_t sr[2][32];
         tmem_ld32(t_s, sr[0]);
@@ -631,15 +670,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         tmem_ld_wait(sr[1]);
         tc_fence_before();
         mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
+        // Only the diagonal block and a ragged last key block need masking: keys
+        // past the causal diagonal or past N get a -inf score, so P = 0 (scale > 0).
+        if ((CAUSAL && j == qblk) || (j + 1) * C::BK > N) {
+          const int lim = (CAUSAL ? min(q, N - 1) : N - 1) - k0;  // keep key k0 + col iff col <= lim
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        }
         const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const int col = 32 * h + c;
             const float2 x = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2, shift2);
-            pf[col] = col <= lim ? ex2(x.x) : 0.f;
-            pf[col + 1] = col + 1 <= lim ? ex2(x.y) : 0.f;
+            pk[(32 * h + c) >> 1] = pack_bf16x2(ex2(x.x), ex2(x.y));
           }
         }
       }
@@ -663,8 +708,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         for (int c = 0; c < 32; c += 2) {
           const int col = 32 * h + c;
           // dS = P (dP - D), with P rounded to bf16 as the other products see it
-          const float2 pb = make_float2(__bfloat162float(__float2bfloat16_rn(pf[col])),
-                                        __bfloat162float(__float2bfloat16_rn(pf[col + 1])));
+          const uint32_t pp = pk[col >> 1];
+          const float2 pb = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u));
           const float2 d = fmul2(pb, fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
           dsk[col >> 1] = pack_bf16x2(d.x, d.y);
         }
@@ -754,7 +799,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, int /*num_sms*/, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs& args, int num_sms, cudaStream_t stream) {
+  BwdArgs a = args;
+  a.head_group = max(1, num_sms / ((a.N + 127) / 128));  // about one wave of CTAs per group
   if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
   return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
 }

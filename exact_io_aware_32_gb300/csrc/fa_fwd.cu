@@ -24,6 +24,7 @@
 // against the same reference, so the final O / l is unchanged in exact
 // arithmetic while most O rescales are skipped.
 #include "fa_internal.h"
+#include "block_order.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -73,8 +74,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
-  const int bh = blockIdx.x;
-  const int qblk = CAUSAL ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.y;
+  int bh, blk;
+  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
+  const int qblk = CAUSAL ? (int)gridDim.y - 1 - blk : blk;  // heaviest first under the causal mask
   const int nkv = (N + C::BN - 1) / C::BN;
   int nb[2];
 #pragma unroll
@@ -112,7 +114,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp waits on the ring barriers; one elected lane issues.
+    if (elect_one()) {
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
@@ -121,33 +124,44 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full, pn * 64,
                       qblk * 256 + t * 128, bh);
-      int nk_issued = 0, nv_issued = 0;
-      for (int j = 0; j < nb_max; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, abort_flag)) break;
+    }
+    __syncwarp();
+    int nk_issued = 0, nv_issued = 0;
+    for (int j = 0; j < nb_max; ++j) {
+      const int s = j % C::kStages;
+      const uint32_t ph = (j / C::kStages) & 1;
+      if (!warp_wait(&bars.k_empty[s], ph ^ 1, abort_flag)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[s],
-                      pn * 64, j * C::BN, bh);
-        nk_issued = j + 1;
-        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, abort_flag)) break;
+          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[s], pn * 64,
+                      j * C::BN, bh);
+      }
+      __syncwarp();
+      nk_issued = j + 1;
+      if (!warp_wait(&bars.v_empty[s], ph ^ 1, abort_flag)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[s],
-                      pn * 64, j * C::BN, bh);
-        nv_issued = j + 1;
+          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[s], pn * 64,
+                      j * C::BN, bh);
       }
-      // Let every issued copy land before the CTA can exit.
-      mbar_wait_drain(&bars.q_full, 0);
-      for (int i = max(0, nk_issued - C::kStages); i < nk_issued; ++i)
-        mbar_wait_drain(&bars.k_full[i % C::kStages], (i / C::kStages) & 1);
-      for (int i = max(0, nv_issued - C::kStages); i < nv_issued; ++i)
-        mbar_wait_drain(&bars.v_full[i % C::kStages], (i / C::kStages) & 1);
+      __syncwarp();
+      nv_issued = j + 1;
     }
+    // Let every issued copy land before the CTA can exit.
+    mbar_wait_drain(&bars.q_full, 0);
+    for (int i = max(0, nk_issued - C::kStages); i < nk_issued; ++i)
+      mbar_wait_drain(&bars.k_full[i % C::kStages], (i / C::kStages) & 1);
+    for (int i = max(0, nv_issued - C::kStages); i < nv_issued; ++i)
+      mbar_wait_drain(&bars.v_full[i % C::kStages], (i / C::kStages) & 1);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp follows the schedule, so it stays converged and its
+    // operands warp-uniform; one elected lane issues each group of tcgen05
+    // ops (elect.sync picks the lowest active lane, so always the same one,
+    // which matters because a commit tracks the issuing thread's MMAs).
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);  // Q, K both K-major
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);       // P from TMEM, V MN-major
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
@@ -157,7 +171,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // add a byte offset / 16 to the start-address field (bits [0,14)).
       const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), dk0 = sdesc_sw128(k_base, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(v_base, C::kPanelBytes, 1024);
-      auto issue_s = [&](int t, int st) {
+      auto issue_s = [&](int t, int st) {  // by the elected lane
         const uint32_t d_s = tmem + C::col_s(t);
         const uint32_t qo = (uint32_t)(t * C::kTileBytes) >> 4, ko = (uint32_t)(st * C::kTileBytes) >> 4;
 #pragma unroll
@@ -167,12 +181,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         mma_commit(&bars.s_full[t]);
       };
-      bool ok = mbar_wait(&bars.q_full, 0, abort_flag) && mbar_wait(&bars.k_full[0], 0, abort_flag);
+      bool ok = warp_wait(&bars.q_full, 0, abort_flag) && warp_wait(&bars.k_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (nb[t] > 0) issue_s(t, 0);
-        mma_commit(&bars.k_empty[0]);
+        if (elect_one()) {
+          for (int t = 0; t < 2; ++t)
+            if (nb[t] > 0) issue_s(t, 0);
+          mma_commit(&bars.k_empty[0]);
+        }
+        __syncwarp();
       }
       // Per key block j and tile t: O_t += P_t V_j, then at once S_t for block
       // j + 1. S_t(j + 1) overwrites the columns P_t(j) occupies; the products
@@ -182,35 +199,43 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       for (int j = 0; ok && j < nb_max; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
-        if (!(ok = mbar_wait(&bars.v_full[s], ph, abort_flag))) break;
+        if (!(ok = warp_wait(&bars.v_full[s], ph, abort_flag))) break;
         const int jn = j + 1, sn = jn % C::kStages;
         bool k_next = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < nb[t]) {
-            if (!(ok = mbar_wait(&bars.p_full[t], j & 1, abort_flag))) break;
+            if (!(ok = warp_wait(&bars.p_full[t], j & 1, abort_flag))) break;
             tc_fence_after();
-            const uint32_t a_p = tmem + C::col_s(t);
-            const uint32_t d_o = tmem + C::col_o(t);
-            const uint32_t vo = (uint32_t)(s * C::kTileBytes) >> 4;
+            if (elect_one()) {
+              const uint32_t a_p = tmem + C::col_s(t);
+              const uint32_t d_o = tmem + C::col_o(t);
+              const uint32_t vo = (uint32_t)(s * C::kTileBytes) >> 4;
 #pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * (2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars.o_done[t]);
+              for (int kk = 0; kk < C::BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * (2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(&bars.o_done[t]);
+            }
+            __syncwarp();
           }
           if (jn < nb[t]) {
             if (!k_next) {
-              if (!(ok = mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, abort_flag))) break;
+              if (!(ok = warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, abort_flag))) break;
               tc_fence_after();
               k_next = true;
             }
-            issue_s(t, sn);
+            if (elect_one()) issue_s(t, sn);
+            __syncwarp();
           }
         }
         if (!ok) break;
-        mma_commit(&bars.v_empty[s]);
-        if (k_next) mma_commit(&bars.k_empty[sn]);
+        if (elect_one()) {
+          mma_commit(&bars.v_empty[s]);
+          if (k_next) mma_commit(&bars.k_empty[sn]);
+        }
+        __syncwarp();
       }
-      mma_commit(&bars.teardown);
+      if (elect_one()) mma_commit(&bars.teardown);
+      __syncwarp();
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
@@ -349,7 +374,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdArgs& a, int /*num_sms*/, cudaStream_t stream) {
+cudaError_t launch_fwd(const FwdArgs& args, int num_sms, cudaStream_t stream) {
+  FwdArgs a = args;
+  a.head_group = max(1, num_sms / ((a.N + 255) / 256));  // about one wave of CTAs per group
   if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
   return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
 }

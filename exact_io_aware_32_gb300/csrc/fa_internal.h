@@ -15,11 +15,11 @@ struct FwdArgs {
   int BH, N, d;
   float scale_log2;  // scale * log2(e)
   int causal;
+  int head_group;  // heads per CTA scheduling group (set by launch_fwd)
 };
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (loads)
-  CUtensorMap tm_q64, tm_do64;          // bf16 [BH][N][d], box 64 x 64 x 1, 128B swizzle (loads)
   CUtensorMap tm_dq, tm_dk, tm_dv;      // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
   const void* o;                        // bf16 [BH][N][d]
   const void* dO;                       // bf16 [BH][N][d]
@@ -29,6 +29,7 @@ struct BwdArgs {
   int BH, N, d;
   float scale, scale_log2;
   int causal;
+  int head_group;  // heads per CTA scheduling group (set by launch_bwd)
 };
 
 // Each returns cudaSuccess or the launch error.

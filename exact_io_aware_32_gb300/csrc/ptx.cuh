@@ -69,6 +69,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait for a whole warp: true only if every lane saw the phase complete,
+// so the warp leaves the wait converged and agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // Teardown wait used to let in-flight copies or MMAs finish before a CTA
 // exits: ignores the abort flag, still bounded by kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
