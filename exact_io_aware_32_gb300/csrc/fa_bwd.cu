@@ -100,26 +100,29 @@ struct DkdvCfg {
   // a 1024-byte boundary (the 128-byte swizzle atoms need it).
   static constexpr int kSmemBytes = kOffBar + 256;
   static constexpr uint32_t kColS = 0;     // S^T fp32
-  static constexpr uint32_t kColDP = 128;  // dP^T fp32; warpgroup w then writes P^T (bf16) over its
-                                           // columns [128 + 64 w, +32) and dS^T over [+32, +64)
+  static constexpr uint32_t kColDP = 128;  // dP^T fp32, then P^T and dS^T as bf16 over it (dkdv_pcol)
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
 };
 
 struct DkdvBarriers {
-  uint64_t kv_full;
+  uint64_t k_full, v_full;
   uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
-  uint64_t s_full, s_free, dp_full, ds_ready, mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, ds_half[2], mma_done, teardown;
   uint32_t tmem_base;
   int abort;
 };
 
 // TMEM column, relative to the dP^T columns, of the packed bf16 operand for
-// k-step kk (16 queries): warpgroup w holds queries [64 w, 64 w + 64) with P^T
-// at [64 w, 64 w + 32) and dS^T at [64 w + 32, 64 w + 64).
+// k-step kk (16 queries). Warpgroup w holds queries [64 w, 64 w + 64) in
+// columns [64 w, 64 w + 64) and finishes them in two halves of 32 queries:
+// half h's fp32 dP^T columns [64 w + 32 h, +32) are replaced by its P^T (16
+// columns of bf16 pairs) followed by its dS^T (16 columns).
 __device__ __forceinline__ uint32_t dkdv_pcol(int kk, bool ds) {
-  return (uint32_t)(64 * (kk >> 2) + (ds ? 32 : 0) + 8 * (kk & 3));
+  return (uint32_t)(64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + (ds ? 16 : 0) + 8 * (kk & 1));
 }
+// k-step of the i-th of the four 16-query steps in query half h: {0, 1, 4, 5} or {2, 3, 6, 7}.
+__device__ __forceinline__ constexpr int dkdv_half_kstep(int h, int i) { return 4 * (i >> 1) + 2 * h + (i & 1); }
 
 // Shared-memory descriptors address the operand start in bits [0,14) as
 // (address >> 4); moving within the same smem window adds to that field.
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
-    mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.k_full, 1);
+    mbar_init(&bars.v_full, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
@@ -160,7 +164,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.ds_ready, 256);
+    mbar_init(&bars.ds_half[0], 256);
+    mbar_init(&bars.ds_half[1], 256);
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
@@ -176,22 +181,22 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // K and V once, then Q and dO of each query block in block order, Q
-    // first (S^T needs it before dP^T needs dO). At d = 128 this is also the
-    // order in which their ring slots come free: dK of block i - 3 releases
-    // Q's slot, then dV of block i - 2 releases dO's. The whole warp waits;
-    // one elected lane issues.
+    // K, then Q and dO of each query block in block order, Q first (S^T
+    // needs it before dP^T needs dO), with V between Q and dO of the first
+    // block, so that the first S^T waits for two tiles only. At d = 128 this
+    // is also the order in which the ring slots come free: dK of block i - 3
+    // releases Q's slot, then dV of block i - 2 releases dO's. The whole warp
+    // waits; one elected lane issues.
     if (elect_one()) {
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_do);
-      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kTileBytes);
-      for (int pn = 0; pn < D / 64; ++pn) {
-        tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.kv_full, pn * 64, kblk * C::BK, bh);
-        tma_load_3d(smem + C::kOffV + pn * kPanelBytes, &a.tm_v, &bars.kv_full, pn * 64, kblk * C::BK, bh);
-      }
+      mbar_arrive_expect_tx(&bars.k_full, C::kTileBytes);
+      for (int pn = 0; pn < D / 64; ++pn)
+        tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.k_full, pn * 64, kblk * C::BK, bh);
     }
     __syncwarp();
     int q_issued = 0, do_issued = 0;
+    bool v_issued = false;
     for (int it = 0; it < n_iter; ++it) {
       const int qs = it % C::kQStages, ds = it % C::kDOStages;
       if (!warp_wait(&bars.q_empty[qs], ((it / C::kQStages) & 1) ^ 1, abort_flag)) break;
@@ -203,6 +208,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       }
       __syncwarp();
       q_issued = it + 1;
+      if (it == 0) {
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars.v_full, C::kTileBytes);
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(smem + C::kOffV + pn * kPanelBytes, &a.tm_v, &bars.v_full, pn * 64, kblk * C::BK, bh);
+        }
+        __syncwarp();
+        v_issued = true;
+      }
       if (!warp_wait(&bars.do_empty[ds], ((it / C::kDOStages) & 1) ^ 1, abort_flag)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars.do_full[ds], C::kTileBytes);
@@ -214,7 +228,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       do_issued = it + 1;
     }
     // let every copy still in flight land before the CTA can exit
-    mbar_wait_drain(&bars.kv_full, 0);
+    mbar_wait_drain(&bars.k_full, 0);
+    if (v_issued) mbar_wait_drain(&bars.v_full, 0);
     for (int i = max(0, q_issued - C::kQStages); i < q_issued; ++i)
       mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
     for (int i = max(0, do_issued - C::kDOStages); i < do_issued; ++i)
@@ -262,35 +277,48 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         __syncwarp();
         return true;
       };
-      // S^T of block i+1 is issued as soon as both warpgroups have read S^T of
-      // block i, so it overlaps their elementwise work. dP^T of block i+1
-      // follows dV and dK of block i in issue order: the products of one
-      // thread execute in that order, so dV and dK have read P^T and dS^T
-      // before dP^T overwrites the columns that hold them.
-      bool ok = warp_wait(&bars.kv_full, 0, abort_flag) && issue_s(0) && issue_dp(0);
+      // Per query block i the critical chain is: the warpgroups' dS^T of block
+      // i -> dV and dK of block i -> dP^T of block i+1 (it overwrites the
+      // columns that hold P^T and dS^T of block i, so it must follow dK in
+      // issue order: the products of one thread execute in that order) -> dS^T
+      // of block i+1. dV and dK start on the first half of the queries while
+      // the warpgroups still work on the second, and S^T of block i+2 goes
+      // after dP^T of block i+1 so that it fills the pipe while the warpgroups
+      // compute dS^T instead of delaying dV and dK.
+      bool ok = warp_wait(&bars.k_full, 0, abort_flag) && issue_s(0) && warp_wait(&bars.v_full, 0, abort_flag) &&
+                issue_dp(0);
+      if (ok && n_iter > 1) ok = warp_wait(&bars.s_free, 0, abort_flag) && issue_s(1);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
-        if (it + 1 < n_iter) {
-          if (!(ok = warp_wait(&bars.s_free, it & 1, abort_flag))) break;
-          if (!(ok = issue_s(it + 1))) break;
-        }
-        if (!(ok = warp_wait(&bars.ds_ready, it & 1, abort_flag))) break;
-        tc_fence_after();
-        if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-            mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
-                   kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.do_empty[ds]);
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = warp_wait(&bars.ds_half[h], it & 1, abort_flag))) break;
+          tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-            mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
-                   kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.q_empty[qs]);
+            for (int i = 0; i < 4; ++i) {  // dK += dS^T Q_i
+              const int kk = dkdv_half_kstep(h, i);
+              mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
+                     kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (h == 1) mma_commit(&bars.q_empty[qs]);  // dK is Q's last reader: its slot refills sooner
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // dV += P^T dO_i
+              const int kk = dkdv_half_kstep(h, i);
+              mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
+                     kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (h == 1) mma_commit(&bars.do_empty[ds]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
         if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
+        if (it + 2 < n_iter) {
+          if (!(ok = warp_wait(&bars.s_free, (it + 1) & 1, abort_flag))) break;
+          if (!(ok = issue_s(it + 2))) break;
+        }
       }
       if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
         mma_commit(&bars.mma_done);
@@ -373,34 +401,35 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      {
-        uint32_t dsk[32];
+      // Two halves of 32 queries: each replaces its own fp32 dP^T columns by
+      // its P^T and dS^T and releases them to the MMA warp at once.
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t dp[32];
-          tmem_ld32(t_dp + 32 * h, dp);
-          tmem_ld_wait(dp);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[32], dsk[16], pkh[16];
+        tmem_ld32(t_dp + 32 * h, dp);
+        tmem_ld_wait(dp);
 #pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const int col = 32 * h + c;
-            const float4 nd = rb4[16 + (col >> 2)];  // -D
-            const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
-            const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
-                                     fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                           make_float2(nd.x, nd.y)));
-            const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
-                                     fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
-                                           make_float2(nd.z, nd.w)));
-            dsk[col >> 1] = pack_bf16x2(d01.x, d01.y);
-            dsk[(col >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
-          }
+        for (int c = 0; c < 32; c += 4) {
+          const int col = 32 * h + c;
+          const float4 nd = rb4[16 + (col >> 2)];  // -D
+          const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
+          const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
+                                   fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                         make_float2(nd.x, nd.y)));
+          const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
+                                   fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                                         make_float2(nd.z, nd.w)));
+          dsk[c >> 1] = pack_bf16x2(d01.x, d01.y);
+          dsk[(c >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
         }
-        tmem_st32(t_dp, pk);        // P^T over dP^T columns this warpgroup has read
-        tmem_st32(t_dp + 32, dsk);  // dS^T next to it
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pkh[i] = pk[16 * h + i];
+        tmem_st16(t_dp + 32 * h, pkh);       // P^T of these queries
+        tmem_st16(t_dp + 32 * h + 16, dsk);  // dS^T of these queries
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.ds_half[h]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars.ds_ready);
     }
     // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK.
     if (ok && n_iter > 0) ok = mbar_wait(&bars.mma_done, 0, abort_flag);
@@ -455,7 +484,7 @@ struct DqCfg {
 };
 
 struct DqBarriers {
-  uint64_t q_full, qt_ready;
+  uint64_t q_full, do_full, qt_ready;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_done, mma_done, teardown;
   uint32_t tmem_base;
@@ -501,6 +530,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.do_full, 1);
     mbar_init(&bars.qt_ready, 256);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
@@ -531,36 +561,56 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // Q, then K and V of each key block, with dO between K and V of the first
+    // block (the first S needs Q and K only). The whole warp waits; one
+    // elected lane issues.
+    if (elect_one()) {
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTileBytes);
-      for (int pn = 0; pn < D / 64; ++pn) {
+      mbar_arrive_expect_tx(&bars.q_full, C::kTileBytes);
+      for (int pn = 0; pn < D / 64; ++pn)
         tma_load_3d(smem + C::kOffQ + pn * kPanelBytes, &a.tm_q, &bars.q_full, pn * 64, qblk * C::BQ, bh);
-        tma_load_3d(smem + C::kOffDO + pn * kPanelBytes, &a.tm_do, &bars.q_full, pn * 64, qblk * C::BQ, bh);
-      }
-      int nk_issued = 0, nv_issued = 0;
-      for (int j = 0; j < nk; ++j) {
-        const int sk = j % C::kKStages, sv = j % C::kVStages;
-        if (!mbar_wait(&bars.k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag)) break;
+    }
+    __syncwarp();
+    int nk_issued = 0, nv_issued = 0;
+    bool do_issued = false;
+    for (int j = 0; j < nk; ++j) {
+      const int sk = j % C::kKStages, sv = j % C::kVStages;
+      if (!warp_wait(&bars.k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
         for (int pn = 0; pn < D / 64; ++pn)
           tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * kPanelBytes, &a.tm_k, &bars.k_full[sk], pn * 64,
                       j * C::BK, bh);
-        nk_issued = j + 1;
-        if (!mbar_wait(&bars.v_empty[sv], ((j / C::kVStages) & 1) ^ 1, abort_flag)) break;
+      }
+      __syncwarp();
+      nk_issued = j + 1;
+      if (j == 0) {
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars.do_full, C::kTileBytes);
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(smem + C::kOffDO + pn * kPanelBytes, &a.tm_do, &bars.do_full, pn * 64, qblk * C::BQ, bh);
+        }
+        __syncwarp();
+        do_issued = true;
+      }
+      if (!warp_wait(&bars.v_empty[sv], ((j / C::kVStages) & 1) ^ 1, abort_flag)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
         for (int pn = 0; pn < D / 64; ++pn)
           tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * kPanelBytes, &a.tm_v, &bars.v_full[sv], pn * 64,
                       j * C::BK, bh);
-        nv_issued = j + 1;
       }
-      mbar_wait_drain(&bars.q_full, 0);
-      for (int i = max(0, nk_issued - C::kKStages); i < nk_issued; ++i)
-        mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
-      for (int i = max(0, nv_issued - C::kVStages); i < nv_issued; ++i)
-        mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
+      __syncwarp();
+      nv_issued = j + 1;
     }
+    // let every copy still in flight land before the CTA can exit
+    mbar_wait_drain(&bars.q_full, 0);
+    if (do_issued) mbar_wait_drain(&bars.do_full, 0);
+    for (int i = max(0, nk_issued - C::kKStages); i < nk_issued; ++i)
+      mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
+    for (int i = max(0, nv_issued - C::kVStages); i < nv_issued; ++i)
+      mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // Whole warp, converged; one elected lane issues (as in the dK/dV kernel).
@@ -604,7 +654,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       // S and dP of block j+1 are issued once the warpgroups have read those of
       // block j; dQ of block j once they have written dS of block j.
       bool ok = warp_wait(&bars.q_full, 0, abort_flag) && warp_wait(&bars.qt_ready, 0, abort_flag) &&
-                issue_s(0) && issue_dp(0);
+                issue_s(0) && warp_wait(&bars.do_full, 0, abort_flag) && issue_dp(0);
       for (int j = 0; ok && j < nk; ++j) {
         if (j + 1 < nk) {
           if (!(ok = warp_wait(&bars.s_free, j & 1, abort_flag))) break;

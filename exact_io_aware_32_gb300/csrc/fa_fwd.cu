@@ -56,7 +56,7 @@ struct FwdCfg {
 };
 
 struct FwdBarriers {
-  uint64_t q_full;
+  uint64_t q_full[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t teardown;
@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
-    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_full[0], 1);
+    mbar_init(&bars.q_full[1], 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -114,18 +115,26 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // The whole warp waits on the ring barriers; one elected lane issues.
+    // Q tile 0, then K and V of each key block, with Q tile 1 between K and
+    // V of the first block (the first S needs Q tile 0 and K only). The whole
+    // warp waits on the ring barriers; one elected lane issues.
+    auto load_q = [&](int t) {
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars.q_full[t], C::kTileBytes);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full[t], pn * 64,
+                      qblk * 256 + t * 128, bh);
+      }
+      __syncwarp();
+    };
     if (elect_one()) {
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full, pn * 64,
-                      qblk * 256 + t * 128, bh);
     }
     __syncwarp();
+    load_q(0);
+    bool q1_issued = false;
     int nk_issued = 0, nv_issued = 0;
     for (int j = 0; j < nb_max; ++j) {
       const int s = j % C::kStages;
@@ -139,6 +148,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       __syncwarp();
       nk_issued = j + 1;
+      if (j == 0) {
+        load_q(1);
+        q1_issued = true;
+      }
       if (!warp_wait(&bars.v_empty[s], ph ^ 1, abort_flag)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
@@ -150,7 +163,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       nv_issued = j + 1;
     }
     // Let every issued copy land before the CTA can exit.
-    mbar_wait_drain(&bars.q_full, 0);
+    mbar_wait_drain(&bars.q_full[0], 0);
+    if (q1_issued) mbar_wait_drain(&bars.q_full[1], 0);
     for (int i = max(0, nk_issued - C::kStages); i < nk_issued; ++i)
       mbar_wait_drain(&bars.k_full[i % C::kStages], (i / C::kStages) & 1);
     for (int i = max(0, nv_issued - C::kStages); i < nv_issued; ++i)
@@ -181,12 +195,17 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
         mma_commit(&bars.s_full[t]);
       };
-      bool ok = warp_wait(&bars.q_full, 0, abort_flag) && warp_wait(&bars.k_full[0], 0, abort_flag);
+      bool ok = warp_wait(&bars.q_full[0], 0, abort_flag) && warp_wait(&bars.k_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one() && nb[0] > 0) issue_s(0, 0);
+        __syncwarp();
+        ok = warp_wait(&bars.q_full[1], 0, abort_flag);
+      }
       if (ok) {
         tc_fence_after();
         if (elect_one()) {
-          for (int t = 0; t < 2; ++t)
-            if (nb[t] > 0) issue_s(t, 0);
+          if (nb[1] > 0) issue_s(1, 0);
           mma_commit(&bars.k_empty[0]);
         }
         __syncwarp();
