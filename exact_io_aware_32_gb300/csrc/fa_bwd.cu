@@ -851,7 +851,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdArgs& args, int num_sms, cudaStream_t stream) {
   BwdArgs a = args;
-  a.head_group = max(1, num_sms / ((a.N + 127) / 128));  // about one wave of CTAs per group
+  // a CTA's fixed cost (loads before the first product, epilogue) is about 2.5 blocks of work
+  a.head_group = pick_head_group(a.BH, (a.N + 127) / 128, a.causal != 0, num_sms, 2.5);
   if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
   return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
 }

@@ -395,7 +395,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdArgs& args, int num_sms, cudaStream_t stream) {
   FwdArgs a = args;
-  a.head_group = max(1, num_sms / ((a.N + 255) / 256));  // about one wave of CTAs per group
+  // a CTA's fixed cost (loads before the first product, epilogue) is about two key blocks of work
+  a.head_group = pick_head_group(a.BH, (a.N + 255) / 256, a.causal != 0, num_sms, 2.0);
   if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
   return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
 }

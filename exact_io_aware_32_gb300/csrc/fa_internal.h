@@ -32,6 +32,10 @@ struct BwdArgs {
   int head_group;  // heads per CTA scheduling group (set by launch_bwd)
 };
 
+// Heads per CTA scheduling group for a (BH x nblk) grid whose causal CTAs
+// cost nblk - blk units of work plus 'overhead' units each (schedule.cu).
+int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead);
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);
