@@ -249,9 +249,13 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), ddo0 = sdesc_sw128(do_base, 16, 1024);
       const uint64_t dqm0 = sdesc_sw128(q_base, kPanelBytes, 1024), ddom0 = sdesc_sw128(do_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
-      auto issue_s = [&](int it) -> bool {  // S^T = K Q_i^T
+      // The issue_* helpers expect their operands' barriers to have been waited
+      // on; the callers pair each with the event the product also waits for
+      // (warp_wait2), since every mbarrier probe costs about a hundred cycles.
+      auto q_phase = [&](int it) { return (uint32_t)((it / C::kQStages) & 1); };
+      auto do_phase = [&](int it) { return (uint32_t)((it / C::kDOStages) & 1); };
+      auto issue_s = [&](int it) {  // S^T = K Q_i^T
         const int s = it % C::kQStages;
-        if (!warp_wait(&bars.q_full[s], (it / C::kQStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
         if (elect_one()) {
@@ -261,11 +265,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           mma_commit(&bars.s_full);
         }
         __syncwarp();
-        return true;
       };
-      auto issue_dp = [&](int it) -> bool {  // dP^T = V dO_i^T
+      auto issue_dp = [&](int it) {  // dP^T = V dO_i^T
         const int s = it % C::kDOStages;
-        if (!warp_wait(&bars.do_full[s], (it / C::kDOStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
         if (elect_one()) {
@@ -275,7 +277,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           mma_commit(&bars.dp_full);
         }
         __syncwarp();
-        return true;
       };
       // Per query block i the critical chain is: the warpgroups' dS^T of block
       // i -> dV and dK of block i -> dP^T of block i+1 (it overwrites the
@@ -285,15 +286,26 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       // the warpgroups still work on the second, and S^T of block i+2 goes
       // after dP^T of block i+1 so that it fills the pipe while the warpgroups
       // compute dS^T instead of delaying dV and dK.
-      bool ok = warp_wait(&bars.k_full, 0, abort_flag) && issue_s(0) && warp_wait(&bars.v_full, 0, abort_flag) &&
-                issue_dp(0);
-      if (ok && n_iter > 1) ok = warp_wait(&bars.s_free, 0, abort_flag) && issue_s(1);
+      bool ok = warp_wait2(&bars.k_full, 0, &bars.q_full[0], 0, abort_flag);
+      if (ok) issue_s(0);
+      ok = ok && warp_wait2(&bars.v_full, 0, &bars.do_full[0], 0, abort_flag);
+      if (ok) issue_dp(0);
+      if (ok && n_iter > 1) {
+        ok = warp_wait2(&bars.s_free, 0, &bars.q_full[1 % C::kQStages], q_phase(1), abort_flag);
+        if (ok) issue_s(1);
+      }
       for (int it = 0; ok && it < n_iter; ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (!(ok = warp_wait(&bars.ds_half[h], it & 1, abort_flag))) break;
+          // the second half's wait also covers dO of the next block, whose dP^T follows
+          if (h == 1 && it + 1 < n_iter)
+            ok = warp_wait2(&bars.ds_half[1], it & 1, &bars.do_full[(it + 1) % C::kDOStages], do_phase(it + 1),
+                            abort_flag);
+          else
+            ok = warp_wait(&bars.ds_half[h], it & 1, abort_flag);
+          if (!ok) break;
           tc_fence_after();
           if (elect_one()) {
 #pragma unroll
@@ -314,10 +326,12 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           __syncwarp();
         }
         if (!ok) break;
-        if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
+        if (it + 1 < n_iter) issue_dp(it + 1);
         if (it + 2 < n_iter) {
-          if (!(ok = warp_wait(&bars.s_free, (it + 1) & 1, abort_flag))) break;
-          if (!(ok = issue_s(it + 2))) break;
+          if (!(ok = warp_wait2(&bars.s_free, (it + 1) & 1, &bars.q_full[(it + 2) % C::kQStages], q_phase(it + 2),
+                                abort_flag)))
+            break;
+          issue_s(it + 2);
         }
       }
       if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
@@ -486,7 +500,7 @@ struct DqCfg {
 struct DqBarriers {
   uint64_t q_full, do_full, qt_ready;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_done, mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, mma_done, teardown;
   uint32_t tmem_base;
   int abort;
 };
@@ -545,7 +559,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.ds_ready, 256);
-    mbar_init(&bars.dq_done, 1);
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
@@ -622,9 +635,12 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       const uint64_t ddo0 = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
       const uint64_t dkm0 = sdesc_sw128(k_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
-      auto issue_s = [&](int j) -> bool {  // S = Q K_j^T
+      // As in the dK/dV kernel, callers wait for the operands (paired with the
+      // event each product also needs).
+      auto k_phase = [&](int j) { return (uint32_t)((j / C::kKStages) & 1); };
+      auto v_phase = [&](int j) { return (uint32_t)((j / C::kVStages) & 1); };
+      auto issue_s = [&](int j) {  // S = Q K_j^T
         const int sk = j % C::kKStages;
-        if (!warp_wait(&bars.k_full[sk], (j / C::kKStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
         if (elect_one()) {
@@ -634,11 +650,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
           mma_commit(&bars.s_full);
         }
         __syncwarp();
-        return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP = dO V_j^T
+      auto issue_dp = [&](int j) {  // dP = dO V_j^T
         const int sv = j % C::kVStages;
-        if (!warp_wait(&bars.v_full[sv], (j / C::kVStages) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
         if (elect_one()) {
@@ -649,18 +663,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
           mma_commit(&bars.v_empty[sv]);
         }
         __syncwarp();
-        return true;
       };
       // S and dP of block j+1 are issued once the warpgroups have read those of
       // block j; dQ of block j once they have written dS of block j.
-      bool ok = warp_wait(&bars.q_full, 0, abort_flag) && warp_wait(&bars.qt_ready, 0, abort_flag) &&
-                issue_s(0) && warp_wait(&bars.do_full, 0, abort_flag) && issue_dp(0);
+      bool ok = warp_wait2(&bars.qt_ready, 0, &bars.k_full[0], 0, abort_flag);
+      if (ok) issue_s(0);
+      ok = ok && warp_wait2(&bars.do_full, 0, &bars.v_full[0], 0, abort_flag);
+      if (ok) issue_dp(0);
       for (int j = 0; ok && j < nk; ++j) {
         if (j + 1 < nk) {
-          if (!(ok = warp_wait(&bars.s_free, j & 1, abort_flag))) break;
-          if (!(ok = issue_s(j + 1))) break;
-          if (!(ok = warp_wait(&bars.dp_free, j & 1, abort_flag))) break;
-          if (!(ok = issue_dp(j + 1))) break;
+          if (!(ok = warp_wait2(&bars.s_free, j & 1, &bars.k_full[(j + 1) % C::kKStages], k_phase(j + 1), abort_flag)))
+            break;
+          issue_s(j + 1);
+          if (!(ok = warp_wait2(&bars.dp_free, j & 1, &bars.v_full[(j + 1) % C::kVStages], v_phase(j + 1), abort_flag)))
+            break;
+          issue_dp(j + 1);
         }
         if (!(ok = warp_wait(&bars.ds_ready, j & 1, abort_flag))) break;
         tc_fence_after();
@@ -670,7 +687,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
           for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
             mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
                    dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.dq_done);
           mma_commit(&bars.k_empty[j % C::kKStages]);
         }
         __syncwarp();
@@ -711,7 +727,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       }
       tc_fence_after();
       const int k0 = j * C::BK + 64 * w;  // first key of this warpgroup's columns
-      uint32_t pk[32];  // P, this thread's row, keys k0 .. k0 + 63, as bf16 pairs
+      float2 pf[32];  // P, this thread's row, keys k0 .. k0 + 63 (fp32: only dS, not P, feeds a product here)
       {
         uint32_t sr[2][32];
         tmem_ld32(t_s, sr[0]);
@@ -734,7 +750,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 x = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2, shift2);
-            pk[(32 * h + c) >> 1] = pack_bf16x2(ex2(x.x), ex2(x.y));
+            pf[(32 * h + c) >> 1] = make_float2(ex2(x.x), ex2(x.y));
           }
         }
       }
@@ -757,15 +773,17 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int col = 32 * h + c;
-          // dS = P (dP - D), with P rounded to bf16 as the other products see it
-          const uint32_t pp = pk[col >> 1];
-          const float2 pb = make_float2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u));
-          const float2 d = fmul2(pb, fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
+          // dS = P (dP - D)
+          const float2 d =
+              fmul2(pf[col >> 1], fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
           dsk[col >> 1] = pack_bf16x2(d.x, d.y);
         }
       }
       if (j > 0) {  // the dQ product of the previous block has read its dS
-        ok = mbar_wait(&bars.dq_done, (j - 1) & 1, abort_flag);
+        // the commit that releases K_{j-1}'s ring slot follows that product; it is the
+        // (j-1) / kKStages-th use of the slot, and the slot cannot be reused before
+        // this thread has stored dS of block j (its next product needs it)
+        ok = mbar_wait(&bars.k_empty[(j - 1) % C::kKStages], ((j - 1) / C::kKStages) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;

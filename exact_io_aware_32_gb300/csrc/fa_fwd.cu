@@ -218,12 +218,18 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       for (int j = 0; ok && j < nb_max; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
-        if (!(ok = warp_wait(&bars.v_full[s], ph, abort_flag))) break;
+        // V of this block is paired with tile 0's P (each mbarrier probe costs
+        // about a hundred cycles; warp_wait2 overlaps the two)
+        if (j < nb[0])
+          ok = warp_wait2(&bars.v_full[s], ph, &bars.p_full[0], j & 1, abort_flag);
+        else
+          ok = warp_wait(&bars.v_full[s], ph, abort_flag);
+        if (!ok) break;
         const int jn = j + 1, sn = jn % C::kStages;
         bool k_next = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < nb[t]) {
-            if (!(ok = warp_wait(&bars.p_full[t], j & 1, abort_flag))) break;
+            if (t == 1 && !(ok = warp_wait(&bars.p_full[t], j & 1, abort_flag))) break;
             tc_fence_after();
             if (elect_one()) {
               const uint32_t a_p = tmem + C::col_s(t);
@@ -232,7 +238,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
               for (int kk = 0; kk < C::BN / 16; ++kk)
                 mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * (2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-              mma_commit(&bars.o_done[t]);
+              // only the epilogue waits for O (the softmax learns of earlier PV products through
+              // the S products issued after them), so only the last one is committed
+              if (j == nb[t] - 1) mma_commit(&bars.o_done[t]);
             }
             __syncwarp();
           }
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
     }
-    if (ok && nbt > 0) ok = mbar_wait(&bars.o_done[t], (nbt - 1) & 1, abort_flag);
+    if (ok && nbt > 0) ok = mbar_wait(&bars.o_done[t], 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (nbt > 0) {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
       uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is no longer read by any MMA

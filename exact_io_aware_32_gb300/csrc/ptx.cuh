@@ -75,6 +75,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
+// warp_wait on two barriers. Each mbarrier probe takes about a hundred
+// cycles even when the phase has completed; probing both before looking at
+// either result overlaps the two latencies in the common case where both
+// phases are already complete.
+__device__ __forceinline__ bool warp_wait2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                           volatile int* abort) {
+  const bool done0 = mbar_try_wait(bar0, parity0);
+  const bool done1 = mbar_try_wait(bar1, parity1);
+  if (__all_sync(0xffffffffu, done0 && done1)) return true;
+  return warp_wait(bar0, parity0, abort) && warp_wait(bar1, parity1, abort);
+}
+
 // Teardown wait used to let in-flight copies or MMAs finish before a CTA
 // exits: ignores the abort flag, still bounded by kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
