@@ -10,14 +10,19 @@ namespace fa {
 // groups of 'group' (about one wave of CTAs): inside a group the block index
 // is the slow coordinate, so the heaviest blocks of the group start first, and
 // all CTAs of a head run at about the same time and share its tiles in L2.
-__device__ __forceinline__ void grouped_block(int BH, int nblk, int group, int& bh, int& blk) {
-  const int linear = (int)(blockIdx.x + blockIdx.y * gridDim.x);  // grid is (BH, nblk)
+// (head, block) of the linear index in that order.
+__device__ __forceinline__ void grouped_index(int linear, int BH, int nblk, int group, int& bh, int& blk) {
   const int per_group = group * nblk;
   const int g = linear / per_group;
   const int idx = linear - g * per_group;
   const int gsize = min(group, BH - g * group);  // the last group may be smaller
   blk = idx / gsize;
   bh = g * group + (idx - blk * gsize);
+}
+
+// The same for the CTA's own linear index in a (BH, nblk) grid.
+__device__ __forceinline__ void grouped_block(int BH, int nblk, int group, int& bh, int& blk) {
+  grouped_index((int)(blockIdx.x + blockIdx.y * gridDim.x), BH, nblk, group, bh, blk);
 }
 
 }  // namespace fa

@@ -128,7 +128,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
   const size_t rows = (size_t)B * H * N;
-  return align256(rows * sizeof(float));
+  return align256(rows * sizeof(float)) + 256;  // D, then the kernels' work counters
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -149,6 +149,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   fa::BwdArgs a;
   std::memset(&a, 0, sizeof(a));
   a.Dsum = static_cast<float*>(workspace);
+  a.work = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + (need - 256));
   if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
       !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||

@@ -31,6 +31,8 @@
 // elementwise work.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "block_order.cuh"
 #include "ptx.cuh"
@@ -42,10 +44,6 @@ using namespace fa::ptx;
 
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
-
-// TMEM column of the packed bf16 operand for k-step kk (16 elements) when
-// warpgroup w wrote elements [64 w, 64 w + 64) at its own columns [64 w, 64 w + 32).
-__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(64 * (kk >> 2) + 8 * (kk & 3)); }
 
 // One 128-byte-swizzled row of a panel: 'nchunks' 16-byte chunks from chunk0.
 __device__ __forceinline__ void st_swizzled_row(uint8_t* panel, int r, int chunk0, const uint32_t* w, int nchunks) {
@@ -123,10 +121,6 @@ __device__ __forceinline__ uint32_t dkdv_pcol(int kk, bool ds) {
 }
 // k-step of the i-th of the four 16-query steps in query half h: {0, 1, 4, 5} or {2, 3, 6, 7}.
 __device__ __forceinline__ constexpr int dkdv_half_kstep(int h, int i) { return 4 * (i >> 1) + 2 * h + (i & 1); }
-
-// Shared-memory descriptors address the operand start in bits [0,14) as
-// (address >> 4); moving within the same smem window adds to that field.
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
@@ -361,18 +355,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       return q < N ? -a.Dsum[(size_t)bh * N + q] : 0.f;
     };
     float next = n_iter > 0 ? fetch(0) : 0.f;
+    // After a failed wait a warp keeps looping without work, so that the
+    // four warps of the group always meet at the same named barriers.
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int q0 = (i_start + it) * C::BQ;
       float* rb = rowbuf + ((it & 1) * 2 + w) * 128;
       rb[tt] = next;
       named_bar_sync(1 + w, 128);
+      if (!ok) continue;
       if (it + 1 < n_iter) next = fetch(it + 1);
       const float4* rb4 = reinterpret_cast<const float4*>(rb);  // lse at [0, 64), D at [64, 128)
       ok = mbar_wait(&bars.s_full, it & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
-        break;
+        continue;
       }
       tc_fence_after();
       uint32_t pk[32];  // P^T row r, queries 64 w .. 64 w + 63, as bf16 pairs
@@ -412,7 +409,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       ok = mbar_wait(&bars.dp_full, it & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
-        break;
+        continue;
       }
       tc_fence_after();
       // Two halves of 32 queries: each replaces its own fp32 dP^T columns by
@@ -472,24 +469,31 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
 }
 
 // ============================================================================ dQ
-// One CTA per 128-row query block (TMEM lane = query), 128 keys per
-// iteration. Q is the same for every key block, so after loading it once the
-// warpgroups copy it into TMEM and S = Q K^T reads its A operand from there.
-// dS has TMEM columns of its own, so S, dP and dQ of consecutive key blocks
-// only wait for the warpgroups to have read the previous tile.
+// Persistent: each CTA takes (head, 128-row query block) tiles from a work
+// counter until none is left; within a tile, TMEM lane = query and each
+// iteration covers 128 keys. Q is the same for every key block of a tile, so
+// the warpgroups copy it into TMEM once and S = Q K^T reads its A operand from
+// there. dS has TMEM columns of its own, so S, dP and dQ of consecutive key
+// blocks only wait for the warpgroups to have read the previous tile.
+//
+// Across tiles the pipeline does not drain: K/V rings and the S/dP/dS barriers
+// count key blocks over the CTA's whole run, the MMA warp issues S and dP of
+// the next tile's first block while the warpgroups write the previous tile's
+// dQ, and the next tile's Q is loaded while the current one is processed.
 template <int D>
 struct DqCfg {
-  static constexpr int BQ = 128;  // queries per CTA
+  static constexpr int BQ = 128;  // queries per tile
   static constexpr int BK = 128;  // keys per iteration
   static constexpr int kTileBytes = (D / 64) * kPanelBytes;
   static constexpr int kKStages = D == 128 ? 3 : 4;
   static constexpr int kVStages = D == 128 ? 2 : 3;
+  static constexpr int kItemSlots = 4;  // tiles fetched ahead by the producer
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTileBytes;
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static constexpr uint32_t kColQ = 0;            // Q, bf16 pairs, D / 2 columns
   static constexpr uint32_t kColDS = D / 2;       // dS, bf16 pairs, 64 columns (warpgroup w: [32 w, 32 w + 32))
   static constexpr uint32_t kColS = D / 2 + 64;   // S fp32, 128 columns
@@ -498,9 +502,13 @@ struct DqCfg {
 };
 
 struct DqBarriers {
-  uint64_t q_full, do_full, qt_ready;
+  uint64_t item_full[4], item_empty[4];  // tile ring: producer -> MMA warp and warpgroups
+  uint64_t q_full, qt_ready;             // Q buffer (one tile) loaded; Q copied into TMEM
+  uint64_t do_full, do_empty;            // dO buffer (one tile)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_tile, teardown;
+  uint64_t ep_staged, dq_stored;        // dQ of a tile staged in the Q buffer; its store has read it
+  int item[4];
   uint32_t tmem_base;
   int abort;
 };
@@ -524,6 +532,21 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
   }
 }
 
+// A dQ tile: (head, query block) and the number of key blocks it sees.
+struct DqTile {
+  int bh, qblk, nk;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq) {
+  DqTile t;
+  int blk;
+  grouped_index(L, a.BH, nq, a.head_group, t.bh, blk);
+  t.qblk = CAUSAL ? nq - 1 - blk : blk;  // heaviest first under the causal mask
+  t.nk = CAUSAL ? t.qblk + 1 : nq;       // BQ == BK: query block i sees key blocks 0..i
+  return t;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<D>;
@@ -535,17 +558,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
   const int nq = (N + C::BQ - 1) / C::BQ;
-  int bh, blk;
-  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
-  const int qblk = CAUSAL ? nq - 1 - blk : blk;  // heaviest first under the causal mask
-  const int nkv = (N + C::BK - 1) / C::BK;
-  const int nk = CAUSAL ? min(qblk + 1, nkv) : nkv;  // key blocks this query block sees
+  const int total = a.BH * nq;
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
+    for (int s = 0; s < C::kItemSlots; ++s) {
+      mbar_init(&bars.item_full[s], 1);
+      mbar_init(&bars.item_empty[s], 1 + 8);  // the MMA warp and the 8 warpgroup warps
+    }
     mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.do_full, 1);
     mbar_init(&bars.qt_ready, 256);
+    mbar_init(&bars.do_full, 1);
+    mbar_init(&bars.do_empty, 1);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -559,7 +583,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_free, 256);
     mbar_init(&bars.ds_ready, 256);
-    mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.dq_tile, 1);
+    mbar_init(&bars.ep_staged, 256);
+    mbar_init(&bars.dq_stored, 1);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
   }
@@ -572,57 +598,126 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
+  // Tile k of this CTA, as published by the producer in the tile ring; -1
+  // (and no further tiles) once the counter is exhausted or on abort. Every
+  // consumer warp reads each slot once and releases it.
+  auto take_tile = [&](int k) -> int {
+    const int is = k % C::kItemSlots;
+    if (!warp_wait(&bars.item_full[is], (k / C::kItemSlots) & 1, abort_flag)) return -1;
+    const int L = *reinterpret_cast<volatile int*>(&bars.item[is]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.item_empty[is]);
+    return L < total ? L : -1;
+  };
+
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // Q, then K and V of each key block, with dO between K and V of the first
-    // block (the first S needs Q and K only). The whole warp waits; one
-    // elected lane issues.
+    // Per tile: its Q, then K and V of each key block, with dO between K and
+    // V of the first block (once the previous tile's last dP has read the dO
+    // buffer). The Q buffer is shared with the dQ epilogue: Q of tile k goes
+    // in once tile k-1's Q is in TMEM and, from k = 2 on, once the dQ of tile
+    // k-2 that the warpgroups staged there has been stored, which this warp
+    // does (so that no warpgroup thread waits on a store). The whole warp
+    // waits; one elected lane issues.
     if (elect_one()) {
       tma_prefetch_desc(&a.tm_k);
       tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars.q_full, C::kTileBytes);
-      for (int pn = 0; pn < D / 64; ++pn)
-        tma_load_3d(smem + C::kOffQ + pn * kPanelBytes, &a.tm_q, &bars.q_full, pn * 64, qblk * C::BQ, bh);
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_do);
     }
     __syncwarp();
-    int nk_issued = 0, nv_issued = 0;
-    bool do_issued = false;
-    for (int j = 0; j < nk; ++j) {
-      const int sk = j % C::kKStages, sv = j % C::kVStages;
-      if (!warp_wait(&bars.k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag)) break;
+    int g = 0;  // key blocks issued over the CTA's run
+    int q_loads = 0, do_loads = 0, k_issued = 0, v_issued = 0;
+    DqTile hist_even = {}, hist_odd = {};  // the last two tiles (by parity of k), for their dQ stores
+    // stores dQ of tile j, staged in the Q buffer, and releases the buffer
+    auto store_dq = [&](int j, bool last) -> bool {
+      if (!warp_wait(&bars.ep_staged, j & 1, abort_flag)) return false;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * kPanelBytes, &a.tm_k, &bars.k_full[sk], pn * 64,
-                      j * C::BK, bh);
+        if (!*abort_flag) {
+          const DqTile tj = (j & 1) ? hist_odd : hist_even;
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_store_3d(&a.tm_dq, smem + C::kOffQ + pn * kPanelBytes, pn * 64, tj.qblk * C::BQ, tj.bh);
+          bulk_commit();
+        }
+        if (last)
+          bulk_wait0();
+        else
+          bulk_wait_read0();
+        mbar_arrive(&bars.dq_stored);
       }
       __syncwarp();
-      nk_issued = j + 1;
-      if (j == 0) {
+      return true;
+    };
+    int ntiles = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int is = k % C::kItemSlots;
+      if (!warp_wait(&bars.item_empty[is], ((k / C::kItemSlots) & 1) ^ 1, abort_flag)) break;
+      int L = 0;
+      if (lane == 0) {
+        L = (int)atomicAdd(&a.work[1], 1u);
+        bars.item[is] = L;
+      }
+      L = __shfl_sync(0xffffffffu, L, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
+      if (L >= total) break;
+      const DqTile t = dq_tile<CAUSAL>(L, a, nq);
+      if (k == 1 && !(ok = warp_wait(&bars.qt_ready, 0, abort_flag))) break;
+      if (k >= 2 && !(ok = store_dq(k - 2, false))) break;
+      if (k & 1)
+        hist_odd = t;
+      else
+        hist_even = t;
+      ntiles = k + 1;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars.q_full, C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffQ + pn * kPanelBytes, &a.tm_q, &bars.q_full, pn * 64, t.qblk * C::BQ, t.bh);
+      }
+      __syncwarp();
+      q_loads = k + 1;
+      for (int j = 0; j < t.nk; ++j, ++g) {
+        const int sk = g % C::kKStages, sv = g % C::kVStages;
+        if (!(ok = warp_wait(&bars.k_empty[sk], ((g / C::kKStages) & 1) ^ 1, abort_flag))) break;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&bars.do_full, C::kTileBytes);
+          mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(smem + C::kOffDO + pn * kPanelBytes, &a.tm_do, &bars.do_full, pn * 64, qblk * C::BQ, bh);
+            tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * kPanelBytes, &a.tm_k, &bars.k_full[sk],
+                        pn * 64, j * C::BK, t.bh);
         }
         __syncwarp();
-        do_issued = true;
+        k_issued = g + 1;
+        if (j == 0) {
+          if (!(ok = warp_wait(&bars.do_empty, (k & 1) ^ 1, abort_flag))) break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&bars.do_full, C::kTileBytes);
+            for (int pn = 0; pn < D / 64; ++pn)
+              tma_load_3d(smem + C::kOffDO + pn * kPanelBytes, &a.tm_do, &bars.do_full, pn * 64, t.qblk * C::BQ,
+                          t.bh);
+          }
+          __syncwarp();
+          do_loads = k + 1;
+        }
+        if (!(ok = warp_wait(&bars.v_empty[sv], ((g / C::kVStages) & 1) ^ 1, abort_flag))) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * kPanelBytes, &a.tm_v, &bars.v_full[sv],
+                        pn * 64, j * C::BK, t.bh);
+        }
+        __syncwarp();
+        v_issued = g + 1;
       }
-      if (!warp_wait(&bars.v_empty[sv], ((j / C::kVStages) & 1) ^ 1, abort_flag)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * kPanelBytes, &a.tm_v, &bars.v_full[sv], pn * 64,
-                      j * C::BK, bh);
-      }
-      __syncwarp();
-      nv_issued = j + 1;
     }
-    // let every copy still in flight land before the CTA can exit
-    mbar_wait_drain(&bars.q_full, 0);
-    if (do_issued) mbar_wait_drain(&bars.do_full, 0);
-    for (int i = max(0, nk_issued - C::kKStages); i < nk_issued; ++i)
+    // the last two tiles' dQ, then every copy still in flight lands before the CTA can exit
+    if (ok && ntiles >= 2) ok = store_dq(ntiles - 2, false);
+    if (ok && ntiles >= 1) ok = store_dq(ntiles - 1, true);
+    if (q_loads > 0) mbar_wait_drain(&bars.q_full, (q_loads - 1) & 1);
+    if (do_loads > 0) mbar_wait_drain(&bars.do_full, (do_loads - 1) & 1);
+    for (int i = max(0, k_issued - C::kKStages); i < k_issued; ++i)
       mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
-    for (int i = max(0, nv_issued - C::kVStages); i < nv_issued; ++i)
+    for (int i = max(0, v_issued - C::kVStages); i < v_issued; ++i)
       mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -635,12 +730,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       const uint64_t ddo0 = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
       const uint64_t dkm0 = sdesc_sw128(k_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
-      // As in the dK/dV kernel, callers wait for the operands (paired with the
-      // event each product also needs).
-      auto k_phase = [&](int j) { return (uint32_t)((j / C::kKStages) & 1); };
-      auto v_phase = [&](int j) { return (uint32_t)((j / C::kVStages) & 1); };
-      auto issue_s = [&](int j) {  // S = Q K_j^T
-        const int sk = j % C::kKStages;
+      auto k_phase = [&](int g) { return (uint32_t)((g / C::kKStages) & 1); };
+      auto v_phase = [&](int g) { return (uint32_t)((g / C::kVStages) & 1); };
+      // The issue_* helpers expect their operands' barriers to have been waited on.
+      auto issue_s = [&](int g) {  // S = Q K_g^T
+        const int sk = g % C::kKStages;
         tc_fence_after();
         const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
         if (elect_one()) {
@@ -651,8 +745,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
         }
         __syncwarp();
       };
-      auto issue_dp = [&](int j) {  // dP = dO V_j^T
-        const int sv = j % C::kVStages;
+      auto issue_dp = [&](int g, bool last_of_tile) {  // dP = dO V_g^T
+        const int sv = g % C::kVStages;
         tc_fence_after();
         const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
         if (elect_one()) {
@@ -661,155 +755,230 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
             mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
           mma_commit(&bars.dp_full);
           mma_commit(&bars.v_empty[sv]);
+          if (last_of_tile) mma_commit(&bars.do_empty);  // the tile's last reader of dO
         }
         __syncwarp();
       };
-      // S and dP of block j+1 are issued once the warpgroups have read those of
-      // block j; dQ of block j once they have written dS of block j.
-      bool ok = warp_wait2(&bars.qt_ready, 0, &bars.k_full[0], 0, abort_flag);
-      if (ok) issue_s(0);
-      ok = ok && warp_wait2(&bars.do_full, 0, &bars.v_full[0], 0, abort_flag);
-      if (ok) issue_dp(0);
-      for (int j = 0; ok && j < nk; ++j) {
-        if (j + 1 < nk) {
-          if (!(ok = warp_wait2(&bars.s_free, j & 1, &bars.k_full[(j + 1) % C::kKStages], k_phase(j + 1), abort_flag)))
-            break;
-          issue_s(j + 1);
-          if (!(ok = warp_wait2(&bars.dp_free, j & 1, &bars.v_full[(j + 1) % C::kVStages], v_phase(j + 1), abort_flag)))
-            break;
-          issue_dp(j + 1);
-        }
-        if (!(ok = warp_wait(&bars.ds_ready, j & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t ko = (uint32_t)((j % C::kKStages) * C::kTileBytes);
-        if (elect_one()) {
+      int k = 0, g = 0;  // tile and key block over the CTA's run
+      int L = take_tile(0);
+      DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
+      bool ok = L >= 0;
+      if (ok) {  // the first tile's first block
+        ok = warp_wait2(&bars.qt_ready, 0, &bars.k_full[0], 0, abort_flag);
+        if (ok) issue_s(0);
+        ok = ok && warp_wait2(&bars.do_full, 0, &bars.v_full[0], 0, abort_flag);
+        if (ok) issue_dp(0, t.nk == 1);
+      }
+      while (ok) {
+        for (int j = 0; ok && j < t.nk; ++j) {
+          const int gj = g + j;
+          if (j + 1 < t.nk) {  // next block of this tile
+            if (!(ok = warp_wait2(&bars.s_free, gj & 1, &bars.k_full[(gj + 1) % C::kKStages], k_phase(gj + 1),
+                                  abort_flag)))
+              break;
+            issue_s(gj + 1);
+            if (!(ok = warp_wait2(&bars.dp_free, gj & 1, &bars.v_full[(gj + 1) % C::kVStages], v_phase(gj + 1),
+                                  abort_flag)))
+              break;
+            issue_dp(gj + 1, j + 1 == t.nk - 1);
+          }
+          if (!(ok = warp_wait(&bars.ds_ready, gj & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t ko = (uint32_t)((gj % C::kKStages) * C::kTileBytes);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-            mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
-                   dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.k_empty[j % C::kKStages]);
+            for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
+              mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
+                     dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.k_empty[gj % C::kKStages]);
+            if (j == t.nk - 1) mma_commit(&bars.dq_tile);
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
+        // The next tile's first block: S needs its Q in TMEM (the warpgroups copy
+        // it after this tile's last block), dP its dO (loaded once this tile's
+        // last dP has read the buffer).
+        g += t.nk;
+        ++k;
+        if ((L = take_tile(k)) < 0) break;
+        t = dq_tile<CAUSAL>(L, a, nq);
+        if (!(ok = warp_wait2(&bars.s_free, (g - 1) & 1, &bars.qt_ready, k & 1, abort_flag) &&
+                   warp_wait(&bars.k_full[g % C::kKStages], k_phase(g), abort_flag)))
+          break;
+        issue_s(g);
+        if (!(ok = warp_wait2(&bars.dp_free, (g - 1) & 1, &bars.do_full, k & 1, abort_flag) &&
+                   warp_wait(&bars.v_full[g % C::kVStages], v_phase(g), abort_flag)))
+          break;
+        issue_dp(g, t.nk == 1);
       }
-      if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
-        mma_commit(&bars.mma_done);
-        mma_commit(&bars.teardown);
-      }
+      if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
       __syncwarp();
       mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
     const int w = warp >> 2;              // key columns [64 w, 64 w + 64) of each block
-    const int r = (warp & 3) * 32 + lane;  // query within the block = TMEM lane
-    const int q = qblk * C::BQ + r;
+    const int r = (warp & 3) * 32 + lane;  // query within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
-    const float lse2 = q < N ? a.lse[(size_t)bh * N + q] * kLog2e : INFINITY;  // rows past N: P = 0
-    const float dsum = q < N ? a.Dsum[(size_t)bh * N + q] : 0.f;
-    // Q into TMEM (row r = lane r): warpgroup w copies the 64-column panel w.
-    bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok && w < D / 64) {
-      tile_row_to_tmem<64>(smem + C::kOffQ + w * kPanelBytes, r, tmem + lane_off + C::kColQ + 32 * w);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    mbar_arrive(&bars.qt_ready);
     const uint32_t t_s = tmem + lane_off + C::kColS + 64 * w;
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;
     const uint32_t t_ds = tmem + lane_off + C::kColDS + 32 * w;
-    for (int j = 0; ok && j < nk; ++j) {
-      ok = mbar_wait(&bars.s_full, j & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
+    // this thread's row terms for a tile, loaded early and converted when
+    // the tile starts (rows past N read row N-1 and get P = 0 then)
+    auto load_row_terms = [&](const DqTile& t, float& lse_raw, float& d_raw) {
+      const int q = min(t.qblk * C::BQ + r, N - 1);
+      lse_raw = a.lse[(size_t)t.bh * N + q];
+      d_raw = a.Dsum[(size_t)t.bh * N + q];
+    };
+    auto row_terms = [&](const DqTile& t, float lse_raw, float d_raw, float& lse2, float& dsum) {
+      const bool in = t.qblk * C::BQ + r < N;
+      lse2 = in ? lse_raw * kLog2e : INFINITY;
+      dsum = in ? d_raw : 0.f;
+    };
+    // Q of tile k into TMEM (row r = lane r): warpgroup w copies the 64-column
+    // panel w. The Q buffer is released separately: after the first tile's
+    // copy at once, later it first stages the previous tile's dQ.
+    auto copy_q = [&](int k) -> bool {
+      bool ok = mbar_wait(&bars.q_full, k & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok && w < D / 64) {
+        tile_row_to_tmem<64>(smem + C::kOffQ + w * kPanelBytes, r, tmem + lane_off + C::kColQ + 32 * w);
+        tmem_st_wait();
       }
-      tc_fence_after();
-      const int k0 = j * C::BK + 64 * w;  // first key of this warpgroup's columns
-      float2 pf[32];  // P, this thread's row, keys k0 .. k0 + 63 (fp32: only dS, not P, feeds a product here)
-      {
-        uint32_t sr[2][32];
-        tmem_ld32(t_s, sr[0]);
-        tmem_ld32(t_s + 32, sr[1]);
-        tmem_ld_wait(sr[0]);
-        tmem_ld_wait(sr[1]);
-        tc_fence_before();
-        mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
-        // Only the diagonal block and a ragged last key block need masking: keys
-        // past the causal diagonal or past N get a -inf score, so P = 0 (scale > 0).
-        if ((CAUSAL && j == qblk) || (j + 1) * C::BK > N) {
-          const int lim = (CAUSAL ? min(q, N - 1) : N - 1) - k0;  // keep key k0 + col iff col <= lim
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-        const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2, shift2);
-            pf[(32 * h + c) >> 1] = make_float2(ex2(x.x), ex2(x.y));
-          }
-        }
-      }
-      ok = mbar_wait(&bars.dp_full, j & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t dp[2][32], dsk[32];
-      tmem_ld32(t_dp, dp[0]);
-      tmem_ld32(t_dp + 32, dp[1]);
-      tmem_ld_wait(dp[0]);
-      tmem_ld_wait(dp[1]);
       tc_fence_before();
-      mbar_arrive(&bars.dp_free);  // dP is in registers: the next block's dP may overwrite it
-      const float2 nd2 = make_float2(-dsum, -dsum);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int col = 32 * h + c;
-          // dS = P (dP - D)
-          const float2 d =
-              fmul2(pf[col >> 1], fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
-          dsk[col >> 1] = pack_bf16x2(d.x, d.y);
-        }
-      }
-      if (j > 0) {  // the dQ product of the previous block has read its dS
-        // the commit that releases K_{j-1}'s ring slot follows that product; it is the
-        // (j-1) / kKStages-th use of the slot, and the slot cannot be reused before
-        // this thread has stored dS of block j (its next product needs it)
-        ok = mbar_wait(&bars.k_empty[(j - 1) % C::kKStages], ((j - 1) / C::kKStages) & 1, abort_flag);
+      mbar_arrive(&bars.qt_ready);
+      return ok;
+    };
+    int k = 0, g = 0;
+    int L = take_tile(0);
+    bool ok = L >= 0;
+    DqTile t = ok ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
+    float lse2 = 0.f, dsum = 0.f;
+    if (ok) {
+      float lr, dr;
+      load_row_terms(t, lr, dr);
+      row_terms(t, lr, dr, lse2, dsum);
+      ok = copy_q(0);
+    }
+    while (ok) {
+      const int q = t.qblk * C::BQ + r;
+      for (int j = 0; j < t.nk; ++j) {
+        const int gj = g + j;
+        ok = mbar_wait(&bars.s_full, gj & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const int k0 = j * C::BK + 64 * w;  // first key of this warpgroup's columns
+        float2 pf[32];  // P, this thread's row, keys k0 .. k0 + 63 (fp32: only dS, not P, feeds a product here)
+        {
+          uint32_t sr[2][32];
+          tmem_ld32(t_s, sr[0]);
+          tmem_ld32(t_s + 32, sr[1]);
+          tmem_ld_wait(sr[0]);
+          tmem_ld_wait(sr[1]);
+          tc_fence_before();
+          mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
+          // Only the diagonal block and a ragged last key block need masking: keys
+          // past the causal diagonal or past N get a -inf score, so P = 0 (scale > 0).
+          if ((CAUSAL && j == t.qblk) || (j + 1) * C::BK > N) {
+            const int lim = (CAUSAL ? min(q, N - 1) : N - 1) - k0;  // keep key k0 + col iff col <= lim
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          }
+          const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-lse2, -lse2);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 x =
+                  ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2, shift2);
+              pf[(32 * h + c) >> 1] = make_float2(ex2(x.x), ex2(x.y));
+            }
+          }
+        }
+        ok = mbar_wait(&bars.dp_full, gj & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dp[2][32], dsk[32];
+        tmem_ld32(t_dp, dp[0]);
+        tmem_ld32(t_dp + 32, dp[1]);
+        tmem_ld_wait(dp[0]);
+        tmem_ld_wait(dp[1]);
+        tc_fence_before();
+        mbar_arrive(&bars.dp_free);  // dP is in registers: the next block's dP may overwrite it
+        const float2 nd2 = make_float2(-dsum, -dsum);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int col = 32 * h + c;
+            // dS = P (dP - D)
+            const float2 d =
+                fmul2(pf[col >> 1], fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
+            dsk[col >> 1] = pack_bf16x2(d.x, d.y);
+          }
+        }
+        if (gj > 0) {
+          // The dQ product of the previous key block has read its dS: the commit
+          // that releases that block's K ring slot follows it. It is the
+          // (gj-1) / kKStages-th use of the slot, and the slot cannot be reused
+          // before this thread has stored dS of this block (the next product
+          // on it needs this dS).
+          ok = mbar_wait(&bars.k_empty[(gj - 1) % C::kKStages], ((gj - 1) / C::kKStages) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(t_ds, dsk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.ds_ready);
       }
-      tmem_st32(t_ds, dsk);
-      tmem_st_wait();
+      if (!ok) break;
+      // The next tile's Q goes into TMEM now (this tile's last S has been read),
+      // so that its first S runs while this tile's dQ is written out; its row
+      // terms are loaded here and converted when it starts.
+      g += t.nk;
+      const DqTile cur = t;
+      L = take_tile(k + 1);
+      DqTile nt = {0, 0, 0};
+      float lse_next = 0.f, d_next = 0.f;
+      if (L >= 0) {
+        nt = dq_tile<CAUSAL>(L, a, nq);
+        load_row_terms(nt, lse_next, d_next);
+        ok = copy_q(k + 1);
+      }
+      // Epilogue of the finished tile: dq = bf16(scale * dQ), staged row by row
+      // in the Q buffer for the producer warp to store; warpgroup w converts
+      // features [D/2 w, D/2 w + D/2). The buffer must hold nothing the
+      // producer still needs: the next tile's Q has been copied out by every
+      // thread, and the previous tile's dQ has been read by its store.
+      bool done = mbar_wait(&bars.dq_tile, k & 1, abort_flag);
+      if (L >= 0) done = done && mbar_wait(&bars.qt_ready, (k + 1) & 1, abort_flag);
+      if (k >= 1) done = done && mbar_wait(&bars.dq_stored, (k - 1) & 1, abort_flag);
+      done = __all_sync(0xffffffffu, done);
+      if (done) {
+        tc_fence_after();
+        stage_row_bf16<D / 2>(tmem + lane_off + C::kColDQ + (D / 2) * w, smem + C::kOffQ, r, (D / 2) * w, a.scale);
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
-      mbar_arrive(&bars.ds_ready);
-    }
-    // Epilogue: dq = bf16(scale * dQ); warpgroup w converts features [D/2 w, D/2 w + D/2).
-    if (ok && nk > 0) ok = mbar_wait(&bars.mma_done, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    uint8_t* stage = smem + C::kOffQ;  // Q in shared memory is not read after the copy into TMEM
-    if (ok && nk > 0) {
-      tc_fence_after();
-      stage_row_bf16<D / 2>(tmem + lane_off + C::kColDQ + (D / 2) * w, stage, r, (D / 2) * w, a.scale);
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, 256);
-    if (threadIdx.x == 0 && nk > 0 && !*abort_flag) {
-      for (int pn = 0; pn < D / 64; ++pn)
-        tma_store_3d(&a.tm_dq, stage + pn * kPanelBytes, pn * 64, qblk * C::BQ, bh);
-      bulk_commit();
-      bulk_wait0();
+      mbar_arrive(&bars.ep_staged);
+      ok = ok && done;
+      if (L < 0) break;
+      t = nt;
+      row_terms(t, lse_next, d_next, lse2, dsum);
+      ++k;
     }
   }
 
@@ -841,10 +1010,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant_
 #pragma unroll
   for (int off = kThreadsPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) a.Dsum[row] = acc;
+  if (blockIdx.x == 0 && threadIdx.x < 2) a.work[threadIdx.x] = 0u;  // tile counters of the next two kernels
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   const long long rows = (long long)a.BH * a.N;
   const int rows_per_block = 256 / (D / 8);
   fa_bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(a);
@@ -861,7 +1031,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  kq<<<dim3((unsigned)a.BH, nblk), 320, DqCfg<D>::kSmemBytes, stream>>>(a);
+  // persistent: one CTA per SM at most (the dQ tiles are handed out by a counter)
+  const long long tiles = (long long)a.BH * nblk;
+  kq<<<(unsigned)std::min<long long>(tiles, num_sms), 320, DqCfg<D>::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -871,8 +1043,9 @@ cudaError_t launch_bwd(const BwdArgs& args, int num_sms, cudaStream_t stream) {
   BwdArgs a = args;
   // a CTA's fixed cost (loads before the first product, epilogue) is about 2.5 blocks of work
   a.head_group = pick_head_group(a.BH, (a.N + 127) / 128, a.causal != 0, num_sms, 2.5);
-  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+  if (a.d == 64)
+    return a.causal ? launch_bwd_t<64, true>(a, num_sms, stream) : launch_bwd_t<64, false>(a, num_sms, stream);
+  return a.causal ? launch_bwd_t<128, true>(a, num_sms, stream) : launch_bwd_t<128, false>(a, num_sms, stream);
 }
 
 }  // namespace fa

@@ -25,6 +25,7 @@ struct BwdArgs {
   const void* dO;                       // bf16 [BH][N][d]
   const float* lse;                     // fp32 [BH][N]
   float* Dsum;                          // fp32 [BH][N], in the caller's workspace
+  unsigned int* work;                   // work counters in the caller's workspace ([0] dK/dV, [1] dQ)
   unsigned int* status;
   int BH, N, d;
   float scale, scale_log2;

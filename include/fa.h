@@ -75,8 +75,9 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: the fp32 row terms
- * D_i = dO_i . o_i [B, H, N], padded to 256 bytes. Returns 0 if the shape is
- * invalid.
+ * D_i = dO_i . o_i [B, H, N], padded to 256 bytes, then 256 bytes of work
+ * counters that the backward kernels use to hand out (head, block) tiles to
+ * their persistent CTAs. Returns 0 if the shape is invalid.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -101,7 +102,7 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
 /*
  * Largest scratch, in bytes, that fa_bwd_noalloc holds per device: the
  * shapes it accepts are those with fa_bwd_workspace_bytes(B, H, N, d) <= this
- * (B * H * N up to 8,388,608 rows).
+ * (B * H * N up to 8,388,544 rows).
  */
 #define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES ((size_t)32 << 20)
 

@@ -41,8 +41,9 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     # fp32 D (one value per row), padded to 256 bytes
-    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 64) == ((2 * 3 * 100 * 4 + 255) // 256) * 256
-    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 128) == 256
+    # fp32 D per row, padded to 256 bytes, then 256 bytes of work counters
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 64) == ((2 * 3 * 100 * 4 + 255) // 256) * 256 + 256
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 128) == 512
     assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
 
