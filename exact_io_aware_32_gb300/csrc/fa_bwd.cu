@@ -75,12 +75,20 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t taddr, uint8_t* tile, in
 }
 
 // ============================================================================ dK / dV
-// One CTA per 128-key block (TMEM lane = key), 128 queries per iteration.
-// Warpgroup w handles queries [64 w, 64 w + 64) of each block and writes P^T
-// and dS^T (bf16) over its own dP^T columns once it has read them.
+// Persistent: each CTA takes (head, 128-key block) tiles from a work counter
+// until none is left. Within a tile, TMEM lane = key and each iteration covers
+// 128 queries; warpgroup w handles queries [64 w, 64 w + 64) of each block and
+// writes P^T and dS^T (bf16) over its own dP^T columns once it has read them.
+//
+// Across tiles the pipeline does not drain: the Q and dO rings and the S/dP/dS
+// barriers count query blocks over the CTA's whole run, the next tile's K and
+// V are loaded once this tile's last S^T and dP^T have read the buffers, and
+// its first products run while the warpgroups write out this tile's dK and dV.
+// The epilogue stages dV and dK as bf16 in the ring slots of the tile's last
+// block; the producer warp stores them with TMA and then releases the slots.
 template <int D>
 struct DkdvCfg {
-  static constexpr int BK = 128;  // keys per CTA
+  static constexpr int BK = 128;  // keys per tile
   static constexpr int BQ = 128;  // queries per iteration
   static constexpr int kTileBytes = (D / 64) * kPanelBytes;
   // Q is needed first in each block (by S^T) and dO later (by dP^T and dV), so
@@ -88,6 +96,7 @@ struct DkdvCfg {
   // completes.
   static constexpr int kQStages = D == 128 ? 3 : 4;
   static constexpr int kDOStages = D == 128 ? 2 : 4;
+  static constexpr int kItemSlots = 4;  // tiles fetched ahead by the producer
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
@@ -96,7 +105,7 @@ struct DkdvCfg {
   static constexpr int kOffBar = kOffRow + 2 * 2 * 128 * 4;
   // No alignment slack: the kernel checks that dynamic shared memory starts on
   // a 1024-byte boundary (the 128-byte swizzle atoms need it).
-  static constexpr int kSmemBytes = kOffBar + 256;
+  static constexpr int kSmemBytes = kOffBar + 512;
   static constexpr uint32_t kColS = 0;     // S^T fp32
   static constexpr uint32_t kColDP = 128;  // dP^T fp32, then P^T and dS^T as bf16 over it (dkdv_pcol)
   static constexpr uint32_t kColDV = 256;
@@ -104,12 +113,20 @@ struct DkdvCfg {
 };
 
 struct DkdvBarriers {
-  uint64_t k_full, v_full;
+  uint64_t item_full[4], item_empty[4];     // tile ring: producer -> MMA warp and warpgroups
+  uint64_t k_full, k_empty, v_full, v_empty;  // K and V buffers (one tile each)
   uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
-  uint64_t s_full, s_free, dp_full, ds_half[2], mma_done, teardown;
+  uint64_t s_full, s_free, dp_full, ds_half[2];
+  uint64_t kv_done, teardown;  // a tile's dV, dK complete
+  // tile j's dV, dK staged in its last ring slots: barrier j % 8, phase j / 8. The
+  // producer stores up to a ring's depth of tiles late, so one barrier waited on
+  // by parity would be ambiguous.
+  uint64_t ep_staged[8];
+  int item[4];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(DkdvBarriers) <= 512, "dK/dV barriers exceed their shared memory");
 
 // TMEM column, relative to the dP^T columns, of the packed bf16 operand for
 // k-step kk (16 queries). Warpgroup w holds queries [64 w, 64 w + 64) in
@@ -121,6 +138,20 @@ __device__ __forceinline__ uint32_t dkdv_pcol(int kk, bool ds) {
 }
 // k-step of the i-th of the four 16-query steps in query half h: {0, 1, 4, 5} or {2, 3, 6, 7}.
 __device__ __forceinline__ constexpr int dkdv_half_kstep(int h, int i) { return 4 * (i >> 1) + 2 * h + (i & 1); }
+
+// A dK/dV tile: (head, key block), its first query block and how many it sees.
+struct DkdvTile {
+  int bh, kblk, i_start, n;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nq) {
+  DkdvTile t;
+  grouped_index(L, a.BH, nq, a.head_group, t.bh, t.kblk);  // key block 0 (the heaviest) first
+  t.i_start = CAUSAL ? t.kblk : 0;                          // BQ == BK: query block i sees key block j iff i >= j
+  t.n = nq - t.i_start;
+  return t;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
@@ -138,15 +169,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
   const int nq = (N + C::BQ - 1) / C::BQ;
-  int bh, kblk;  // key block 0 has the most query blocks under the causal mask: it goes first
-  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, kblk);
-  const int i_start = CAUSAL ? kblk : 0;  // BQ == BK: query block i sees key block j iff i >= j
-  const int n_iter = nq - i_start;
+  const int total = a.BH * nq;
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
+    for (int s = 0; s < C::kItemSlots; ++s) {
+      mbar_init(&bars.item_full[s], 1);
+      mbar_init(&bars.item_empty[s], 1 + 8);  // the MMA warp and the 8 warpgroup warps
+    }
     mbar_init(&bars.k_full, 1);
+    mbar_init(&bars.k_empty, 1);
     mbar_init(&bars.v_full, 1);
+    mbar_init(&bars.v_empty, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
@@ -160,7 +194,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_half[0], 256);
     mbar_init(&bars.ds_half[1], 256);
-    mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.kv_done, 1);
+    for (int j = 0; j < 8; ++j) mbar_init(&bars.ep_staged[j], 256);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
   }
@@ -173,57 +208,143 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
+  // Tile k of this CTA, as published by the producer in the tile ring; -1 once
+  // the counter is exhausted. Every consumer warp reads each slot once and
+  // releases it. The wait ignores the abort flag (bounded by time only), so
+  // that the warps of a warpgroup agree on their sequence of tiles.
+  auto take_tile = [&](int k) -> int {
+    const int is = k % C::kItemSlots;
+    const bool got = __all_sync(0xffffffffu, mbar_wait_drain(&bars.item_full[is], (k / C::kItemSlots) & 1));
+    if (!got) {
+      *abort_flag = 1;
+      return -1;
+    }
+    const int L = *reinterpret_cast<volatile int*>(&bars.item[is]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.item_empty[is]);
+    return L < total ? L : -1;
+  };
+
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // K, then Q and dO of each query block in block order, Q first (S^T
-    // needs it before dP^T needs dO), with V between Q and dO of the first
-    // block, so that the first S^T waits for two tiles only. At d = 128 this
-    // is also the order in which the ring slots come free: dK of block i - 3
-    // releases Q's slot, then dV of block i - 2 releases dO's. The whole warp
-    // waits; one elected lane issues.
+    // Per tile: K, then Q and dO of each query block in block order (Q first:
+    // S^T needs it before dP^T needs dO), with V between Q and dO of the first
+    // block. K and V wait for the previous tile's last S^T and dP^T. A ring
+    // slot that held a tile's last block holds its staged dV or dK next: the
+    // producer stores them (when the slot is about to be reused) and then
+    // releases the slots itself. The whole warp waits; one elected lane issues.
     if (elect_one()) {
       tma_prefetch_desc(&a.tm_q);
       tma_prefetch_desc(&a.tm_do);
-      mbar_arrive_expect_tx(&bars.k_full, C::kTileBytes);
-      for (int pn = 0; pn < D / 64; ++pn)
-        tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.k_full, pn * 64, kblk * C::BK, bh);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
     }
     __syncwarp();
-    int q_issued = 0, do_issued = 0;
-    bool v_issued = false;
-    for (int it = 0; it < n_iter; ++it) {
-      const int qs = it % C::kQStages, ds = it % C::kDOStages;
-      if (!warp_wait(&bars.q_empty[qs], ((it / C::kQStages) & 1) ^ 1, abort_flag)) break;
+    DkdvTile hist[8];  // recent tiles (by k & 7) and the global index of their last block
+    int hist_last[8];
+    int g = 0, ntiles = 0, next_store = 0;
+    int q_issued = 0, do_issued = 0, kv_tiles = 0;
+    bool ok = true;
+    // store tile j's staged dV (dO slot of its last block) and dK (Q slot)
+    auto store_tile = [&](int j, bool last) -> bool {
+      if (!warp_wait(&bars.ep_staged[j & 7], (j >> 3) & 1, abort_flag)) return false;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.q_full[qs], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffQ + qs * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.q_full[qs], pn * 64,
-                      (i_start + it) * C::BQ, bh);
+        const DkdvTile tj = hist[j & 7];
+        const int gl = hist_last[j & 7];
+        uint8_t* dv_stage = smem + C::kOffDO + (gl % C::kDOStages) * C::kTileBytes;
+        uint8_t* dk_stage = smem + C::kOffQ + (gl % C::kQStages) * C::kTileBytes;
+        if (!*abort_flag) {
+          for (int pn = 0; pn < D / 64; ++pn) {
+            tma_store_3d(&a.tm_dv, dv_stage + pn * kPanelBytes, pn * 64, tj.kblk * C::BK, tj.bh);
+            tma_store_3d(&a.tm_dk, dk_stage + pn * kPanelBytes, pn * 64, tj.kblk * C::BK, tj.bh);
+          }
+          bulk_commit();
+        }
+        if (last)
+          bulk_wait0();
+        else
+          bulk_wait_read0();
+        mbar_arrive(&bars.do_empty[gl % C::kDOStages]);  // in place of the MMA warp's release
+        mbar_arrive(&bars.q_empty[gl % C::kQStages]);
       }
       __syncwarp();
-      q_issued = it + 1;
-      if (it == 0) {
+      return true;
+    };
+    // before block g reuses a slot of a ring with 'stages' slots
+    auto store_due = [&](int g_next, int stages) -> bool {
+      while (next_store < ntiles && hist_last[next_store & 7] + stages <= g_next) {
+        if (!store_tile(next_store, false)) return false;
+        ++next_store;
+      }
+      return true;
+    };
+    for (int k = 0; ok; ++k) {
+      const int is = k % C::kItemSlots;
+      if (!warp_wait(&bars.item_empty[is], ((k / C::kItemSlots) & 1) ^ 1, abort_flag)) break;
+      int L = 0;
+      if (lane == 0) {
+        L = (int)atomicAdd(&a.work[0], 1u);
+        bars.item[is] = L;
+      }
+      L = __shfl_sync(0xffffffffu, L, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
+      if (L >= total) break;
+      const DkdvTile t = dkdv_tile<CAUSAL>(L, a, nq);
+      hist[k & 7] = t;
+      hist_last[k & 7] = g + t.n - 1;
+      ntiles = k + 1;
+      if (k >= 1 && !(ok = warp_wait(&bars.k_empty, (k - 1) & 1, abort_flag))) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars.k_full, C::kTileBytes);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(smem + C::kOffK + pn * kPanelBytes, &a.tm_k, &bars.k_full, pn * 64, t.kblk * C::BK, t.bh);
+      }
+      __syncwarp();
+      kv_tiles = k + 1;
+      for (int it = 0; it < t.n; ++it, ++g) {
+        const int qs = g % C::kQStages, ds = g % C::kDOStages;
+        if (!(ok = store_due(g, C::kQStages))) break;
+        if (!(ok = warp_wait(&bars.q_empty[qs], ((g / C::kQStages) & 1) ^ 1, abort_flag))) break;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&bars.v_full, C::kTileBytes);
+          mbar_arrive_expect_tx(&bars.q_full[qs], C::kTileBytes);
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(smem + C::kOffV + pn * kPanelBytes, &a.tm_v, &bars.v_full, pn * 64, kblk * C::BK, bh);
+            tma_load_3d(smem + C::kOffQ + qs * C::kTileBytes + pn * kPanelBytes, &a.tm_q, &bars.q_full[qs],
+                        pn * 64, (t.i_start + it) * C::BQ, t.bh);
         }
         __syncwarp();
-        v_issued = true;
+        q_issued = g + 1;
+        if (it == 0) {
+          if (k >= 1 && !(ok = warp_wait(&bars.v_empty, (k - 1) & 1, abort_flag))) break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&bars.v_full, C::kTileBytes);
+            for (int pn = 0; pn < D / 64; ++pn)
+              tma_load_3d(smem + C::kOffV + pn * kPanelBytes, &a.tm_v, &bars.v_full, pn * 64, t.kblk * C::BK,
+                          t.bh);
+          }
+          __syncwarp();
+        }
+        if (!(ok = store_due(g, C::kDOStages))) break;
+        if (!(ok = warp_wait(&bars.do_empty[ds], ((g / C::kDOStages) & 1) ^ 1, abort_flag))) break;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(&bars.do_full[ds], C::kTileBytes);
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(smem + C::kOffDO + ds * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.do_full[ds],
+                        pn * 64, (t.i_start + it) * C::BQ, t.bh);
+        }
+        __syncwarp();
+        do_issued = g + 1;
       }
-      if (!warp_wait(&bars.do_empty[ds], ((it / C::kDOStages) & 1) ^ 1, abort_flag)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.do_full[ds], C::kTileBytes);
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_load_3d(smem + C::kOffDO + ds * C::kTileBytes + pn * kPanelBytes, &a.tm_do, &bars.do_full[ds],
-                      pn * 64, (i_start + it) * C::BQ, bh);
-      }
-      __syncwarp();
-      do_issued = it + 1;
     }
-    // let every copy still in flight land before the CTA can exit
-    mbar_wait_drain(&bars.k_full, 0);
-    if (v_issued) mbar_wait_drain(&bars.v_full, 0);
+    // the tiles still staged, the last with a full wait; then every copy in flight lands
+    while (ok && next_store < ntiles) {
+      ok = store_tile(next_store, next_store == ntiles - 1);
+      ++next_store;
+    }
+    if (kv_tiles > 0) {
+      mbar_wait_drain(&bars.k_full, (kv_tiles - 1) & 1);
+      mbar_wait_drain(&bars.v_full, (kv_tiles - 1) & 1);
+    }
     for (int i = max(0, q_issued - C::kQStages); i < q_issued; ++i)
       mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
     for (int i = max(0, do_issued - C::kDOStages); i < do_issued; ++i)
@@ -237,19 +358,41 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV, dK: A from TMEM, B MN-major
       const uint32_t k_base = smem_u32(smem + C::kOffK), v_base = smem_u32(smem + C::kOffV);
       const uint32_t q_base = smem_u32(smem + C::kOffQ), do_base = smem_u32(smem + C::kOffDO);
-      // Descriptors of stage 0; k-steps and stage 1 add a byte offset / 16 to the
-      // start-address field (bits [0,14)).
+      // Descriptors of stage 0; k-steps and other stages add a byte offset / 16 to
+      // the start-address field (bits [0,14)).
       const uint64_t dk0 = sdesc_sw128(k_base, 16, 1024), dv0 = sdesc_sw128(v_base, 16, 1024);
       const uint64_t dq0 = sdesc_sw128(q_base, 16, 1024), ddo0 = sdesc_sw128(do_base, 16, 1024);
       const uint64_t dqm0 = sdesc_sw128(q_base, kPanelBytes, 1024), ddom0 = sdesc_sw128(do_base, kPanelBytes, 1024);
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
-      // The issue_* helpers expect their operands' barriers to have been waited
-      // on; the callers pair each with the event the product also waits for
-      // (warp_wait2), since every mbarrier probe costs about a hundred cycles.
-      auto q_phase = [&](int it) { return (uint32_t)((it / C::kQStages) & 1); };
-      auto do_phase = [&](int it) { return (uint32_t)((it / C::kDOStages) & 1); };
-      auto issue_s = [&](int it) {  // S^T = K Q_i^T
-        const int s = it % C::kQStages;
+      auto q_phase = [&](int g) { return (uint32_t)((g / C::kQStages) & 1); };
+      auto do_phase = [&](int g) { return (uint32_t)((g / C::kDOStages) & 1); };
+      // Blocks in run order as (position in the tile, tile size, tile index in
+      // the run); n == 0 past the end of the run. The loop keeps blocks g and
+      // g+1 in registers and takes g+2 after dP^T of block g+1 is issued.
+      struct Blk {
+        int it, n, kt;
+      };
+      Blk cursor = {0, 0, -1};  // the block last handed out
+      bool tiles_done = false;
+      auto next_blk = [&]() -> Blk {
+        if (cursor.it + 1 < cursor.n) {
+          ++cursor.it;
+          return cursor;
+        }
+        const int L = tiles_done ? -1 : take_tile(cursor.kt + 1);
+        if (L < 0) {
+          tiles_done = true;
+          return Blk{0, 0, -1};
+        }
+        cursor = Blk{0, dkdv_tile<CAUSAL>(L, a, nq).n, cursor.kt + 1};
+        return cursor;
+      };
+      auto issue_s = [&](int g, bool first, bool last, int kt) -> bool {  // S^T = K Q_i^T
+        const int s = g % C::kQStages;
+        bool ok = g == 0 ? warp_wait(&bars.q_full[s], q_phase(g), abort_flag)
+                         : warp_wait2(&bars.s_free, (g - 1) & 1, &bars.q_full[s], q_phase(g), abort_flag);
+        if (ok && first) ok = warp_wait(&bars.k_full, kt & 1, abort_flag);
+        if (!ok) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
         if (elect_one()) {
@@ -257,11 +400,18 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
           mma_commit(&bars.s_full);
+          if (last) mma_commit(&bars.k_empty);  // the tile's last reader of K
         }
         __syncwarp();
+        return true;
       };
-      auto issue_dp = [&](int it) {  // dP^T = V dO_i^T
-        const int s = it % C::kDOStages;
+      // do_waited: the caller has already waited for this block's dO (a tile's first block also needs V)
+      auto issue_dp = [&](int g, bool first, bool last, int kt, bool do_waited) -> bool {  // dP^T = V dO_i^T
+        const int s = g % C::kDOStages;
+        bool ok = first       ? warp_wait2(&bars.do_full[s], do_phase(g), &bars.v_full, kt & 1, abort_flag)
+                  : do_waited ? true
+                              : warp_wait(&bars.do_full[s], do_phase(g), abort_flag);
+        if (!ok) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
         if (elect_one()) {
@@ -269,8 +419,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
           mma_commit(&bars.dp_full);
+          if (last) mma_commit(&bars.v_empty);  // the tile's last reader of V
         }
         __syncwarp();
+        return true;
       };
       // Per query block i the critical chain is: the warpgroups' dS^T of block
       // i -> dV and dK of block i -> dP^T of block i+1 (it overwrites the
@@ -279,26 +431,30 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       // of block i+1. dV and dK start on the first half of the queries while
       // the warpgroups still work on the second, and S^T of block i+2 goes
       // after dP^T of block i+1 so that it fills the pipe while the warpgroups
-      // compute dS^T instead of delaying dV and dK.
-      bool ok = warp_wait2(&bars.k_full, 0, &bars.q_full[0], 0, abort_flag);
-      if (ok) issue_s(0);
-      ok = ok && warp_wait2(&bars.v_full, 0, &bars.do_full[0], 0, abort_flag);
-      if (ok) issue_dp(0);
-      if (ok && n_iter > 1) {
-        ok = warp_wait2(&bars.s_free, 0, &bars.q_full[1 % C::kQStages], q_phase(1), abort_flag);
-        if (ok) issue_s(1);
+      // compute dS^T instead of delaying dV and dK. A tile's first S^T waits
+      // until the previous tile's last block (its K buffer then has had a
+      // block's time to refill).
+      Blk b0 = next_blk(), b1 = {0, 0, -1};
+      bool ok = b0.n > 0;
+      if (ok) {
+        ok = issue_s(0, true, b0.n == 1, b0.kt) && issue_dp(0, true, b0.n == 1, b0.kt, false);
+        b1 = next_blk();
+        if (ok && b1.it > 0) ok = issue_s(1, false, b1.it == b1.n - 1, b1.kt);
       }
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+      for (int g = 0; ok && b0.n > 0; ++g) {
+        const int it = b0.it;
+        const int qs = g % C::kQStages, ds = g % C::kDOStages;
         const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
+        const bool last = it == b0.n - 1;
+        // the second half's wait also covers dO of the next block of the tile, whose dP^T follows
+        const bool pair_do = !last;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          // the second half's wait also covers dO of the next block, whose dP^T follows
-          if (h == 1 && it + 1 < n_iter)
-            ok = warp_wait2(&bars.ds_half[1], it & 1, &bars.do_full[(it + 1) % C::kDOStages], do_phase(it + 1),
+          if (h == 1 && pair_do)
+            ok = warp_wait2(&bars.ds_half[1], g & 1, &bars.do_full[(g + 1) % C::kDOStages], do_phase(g + 1),
                             abort_flag);
           else
-            ok = warp_wait(&bars.ds_half[h], it & 1, abort_flag);
+            ok = warp_wait(&bars.ds_half[h], g & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           if (elect_one()) {
@@ -308,30 +464,33 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
               mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
                      kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
             }
-            if (h == 1) mma_commit(&bars.q_empty[qs]);  // dK is Q's last reader: its slot refills sooner
+            // dK is Q's last reader: its slot refills sooner (a tile's last slots
+            // are released by the producer once their staged dK, dV are stored)
+            if (h == 1 && !last) mma_commit(&bars.q_empty[qs]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // dV += P^T dO_i
               const int kk = dkdv_half_kstep(h, i);
               mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
                      kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
             }
-            if (h == 1) mma_commit(&bars.do_empty[ds]);
+            if (h == 1) mma_commit(last ? &bars.kv_done : &bars.do_empty[ds]);
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (it + 1 < n_iter) issue_dp(it + 1);
-        if (it + 2 < n_iter) {
-          if (!(ok = warp_wait2(&bars.s_free, (it + 1) & 1, &bars.q_full[(it + 2) % C::kQStages], q_phase(it + 2),
-                                abort_flag)))
-            break;
-          issue_s(it + 2);
+        // block g+1: its dP^T (and its S^T first if it starts a tile); block g+2: its S^T unless it starts one
+        Blk b2 = {0, 0, -1};
+        if (b1.n > 0) {
+          const bool first1 = b1.it == 0, last1 = b1.it == b1.n - 1;
+          if (first1 && !(ok = issue_s(g + 1, true, last1, b1.kt))) break;
+          if (!(ok = issue_dp(g + 1, first1, last1, b1.kt, pair_do))) break;
+          b2 = next_blk();
+          if (b2.it > 0 && !(ok = issue_s(g + 2, false, b2.it == b2.n - 1, b2.kt))) break;
         }
+        b0 = b1;
+        b1 = b2;
       }
-      if (elect_one()) {  // the same lane as above: elect.sync picks the lowest active lane
-        mma_commit(&bars.mma_done);
-        mma_commit(&bars.teardown);
-      }
+      if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
       __syncwarp();
       mbar_wait_drain(&bars.teardown, 0);
     }
@@ -340,125 +499,145 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const int w = warp >> 2;              // columns (queries) [64 w, 64 w + 64) of each block
     const int r = (warp & 3) * 32 + lane;  // key within the block = TMEM lane
     const int tt = threadIdx.x & 127;
-    const int key = kblk * C::BK + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS + 64 * w;
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;  // dP^T, then P^T | dS^T (bf16)
     const float sl2 = a.scale_log2;
-    const bool key_ok = key < N;
-    const bool keys_all_ok = (kblk + 1) * C::BK <= N;  // uniform over the CTA
     // Threads 0-63 of the warpgroup fetch -lse (log2 units) of the group's 64
-    // queries, threads 64-127 fetch -D; one block ahead, through registers.
-    auto fetch = [&](int it) -> float {
-      const int q = (i_start + it) * C::BQ + 64 * w + (tt & 63);
-      if (tt < 64) return q < N ? -a.lse[(size_t)bh * N + q] * kLog2e : -INFINITY;  // 2^(x - inf) = 0 past N
-      return q < N ? -a.Dsum[(size_t)bh * N + q] : 0.f;
+    // queries of query block qb, threads 64-127 fetch -D; one block ahead,
+    // through registers.
+    auto fetch = [&](const DkdvTile& t, int qb) -> float {
+      const int q = qb * C::BQ + 64 * w + (tt & 63);
+      if (tt < 64) return q < N ? -a.lse[(size_t)t.bh * N + q] * kLog2e : -INFINITY;  // 2^(x - inf) = 0 past N
+      return q < N ? -a.Dsum[(size_t)t.bh * N + q] : 0.f;
     };
-    float next = n_iter > 0 ? fetch(0) : 0.f;
-    // After a failed wait a warp keeps looping without work, so that the
-    // four warps of the group always meet at the same named barriers.
-    bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
-      const int q0 = (i_start + it) * C::BQ;
-      float* rb = rowbuf + ((it & 1) * 2 + w) * 128;
-      rb[tt] = next;
-      named_bar_sync(1 + w, 128);
-      if (!ok) continue;
-      if (it + 1 < n_iter) next = fetch(it + 1);
-      const float4* rb4 = reinterpret_cast<const float4*>(rb);  // lse at [0, 64), D at [64, 128)
-      ok = mbar_wait(&bars.s_full, it & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        continue;
-      }
-      tc_fence_after();
-      uint32_t pk[32];  // P^T row r, queries 64 w .. 64 w + 63, as bf16 pairs
-      {
-        uint32_t sr[2][32];
-        tmem_ld32(t_s, sr[0]);
-        tmem_ld32(t_s + 32, sr[1]);
-        tmem_ld_wait(sr[0]);
-        tmem_ld_wait(sr[1]);
-        tc_fence_before();
-        mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
-        // Only the diagonal block (the first under the causal mask) and a ragged
-        // last key block need masking: there a hidden score becomes -inf, so P = 0
-        // (scale > 0). Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col >= key.
-        if ((CAUSAL && it == 0) || !keys_all_ok) {
-          const int lim = CAUSAL && it == 0 ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < lim || !key_ok) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-        const float2 scale2 = make_float2(sl2, sl2);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const int col = 32 * h + c;  // within the group's 64 queries
-            const float4 nl = rb4[col >> 2];  // -lse
-            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), scale2,
-                                     make_float2(nl.x, nl.y));
-            const float2 x23 = ffma2(make_float2(__uint_as_float(sr[h][c + 2]), __uint_as_float(sr[h][c + 3])),
-                                     scale2, make_float2(nl.z, nl.w));
-            pk[col >> 1] = pack_bf16x2(ex2(x01.x), ex2(x01.y));
-            pk[(col >> 1) + 1] = pack_bf16x2(ex2(x23.x), ex2(x23.y));
+    // After a failed wait a warp keeps going without work; at every block the
+    // group's named barrier also ANDs the warps' states, so the four warps
+    // always agree on their blocks and tiles and meet at the same barriers.
+    int L = take_tile(0);
+    DkdvTile t = L >= 0 ? dkdv_tile<CAUSAL>(L, a, nq) : DkdvTile{0, 0, 0, 0};
+    float next = L >= 0 ? fetch(t, t.i_start) : 0.f;
+    bool ok = L >= 0;
+    int g = 0;
+    for (int k = 0; L >= 0; ++k) {
+      const int key = t.kblk * C::BK + r;
+      const bool key_ok = key < N;
+      const bool keys_all_ok = (t.kblk + 1) * C::BK <= N;  // uniform over the CTA
+      int L_next = -1;
+      DkdvTile nt = {0, 0, 0, 0};
+      for (int it = 0; it < t.n; ++it, ++g) {
+        const int q0 = (t.i_start + it) * C::BQ;
+        float* rb = rowbuf + ((g & 1) * 2 + w) * 128;
+        rb[tt] = next;
+        ok = named_bar_and(1 + w, 128, ok);
+        if (it + 1 < t.n) {
+          next = fetch(t, t.i_start + it + 1);
+        } else {  // the next tile's first block
+          L_next = take_tile(k + 1);
+          if (L_next >= 0) {
+            nt = dkdv_tile<CAUSAL>(L_next, a, nq);
+            next = fetch(nt, nt.i_start);
           }
         }
-      }
-      ok = mbar_wait(&bars.dp_full, it & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        continue;
-      }
-      tc_fence_after();
-      // Two halves of 32 queries: each replaces its own fp32 dP^T columns by
-      // its P^T and dS^T and releases them to the MMA warp at once.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t dp[32], dsk[16], pkh[16];
-        tmem_ld32(t_dp + 32 * h, dp);
-        tmem_ld_wait(dp);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const int col = 32 * h + c;
-          const float4 nd = rb4[16 + (col >> 2)];  // -D
-          const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
-          const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
-                                   fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                         make_float2(nd.x, nd.y)));
-          const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
-                                   fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
-                                         make_float2(nd.z, nd.w)));
-          dsk[c >> 1] = pack_bf16x2(d01.x, d01.y);
-          dsk[(c >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
+        if (!ok) continue;
+        const float4* rb4 = reinterpret_cast<const float4*>(rb);  // lse at [0, 64), D at [64, 128)
+        ok = mbar_wait(&bars.s_full, g & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          continue;
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pkh[i] = pk[16 * h + i];
-        tmem_st16(t_dp + 32 * h, pkh);       // P^T of these queries
-        tmem_st16(t_dp + 32 * h + 16, dsk);  // dS^T of these queries
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars.ds_half[h]);
-      }
-    }
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK.
-    if (ok && n_iter > 0) ok = mbar_wait(&bars.mma_done, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    if (n_iter > 0) {
-      uint8_t* stage = smem + (w == 0 ? C::kOffQ : C::kOffDO);  // free once every product has completed
-      if (ok) {
         tc_fence_after();
+        uint32_t pk[32];  // P^T row r, queries 64 w .. 64 w + 63, as bf16 pairs
+        {
+          uint32_t sr[2][32];
+          tmem_ld32(t_s, sr[0]);
+          tmem_ld32(t_s + 32, sr[1]);
+          tmem_ld_wait(sr[0]);
+          tmem_ld_wait(sr[1]);
+          tc_fence_before();
+          mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
+          // Only the diagonal block (the first under the causal mask) and a ragged
+          // last key block need masking: there a hidden score becomes -inf, so P = 0
+          // (scale > 0). Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col >= key.
+          if ((CAUSAL && it == 0) || !keys_all_ok) {
+            const int lim = CAUSAL && it == 0 ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < lim || !key_ok) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+          }
+          const float2 scale2 = make_float2(sl2, sl2);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const int col = 32 * h + c;  // within the group's 64 queries
+              const float4 nl = rb4[col >> 2];  // -lse
+              const float2 x01 = ffma2(make_float2(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])),
+                                       scale2, make_float2(nl.x, nl.y));
+              const float2 x23 = ffma2(make_float2(__uint_as_float(sr[h][c + 2]), __uint_as_float(sr[h][c + 3])),
+                                       scale2, make_float2(nl.z, nl.w));
+              pk[col >> 1] = pack_bf16x2(ex2(x01.x), ex2(x01.y));
+              pk[(col >> 1) + 1] = pack_bf16x2(ex2(x23.x), ex2(x23.y));
+            }
+          }
+        }
+        ok = mbar_wait(&bars.dp_full, g & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          continue;
+        }
+        tc_fence_after();
+        // Two halves of 32 queries: each replaces its own fp32 dP^T columns by
+        // its P^T and dS^T and releases them to the MMA warp at once.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t dp[32], dsk[16], pkh[16];
+          tmem_ld32(t_dp + 32 * h, dp);
+          tmem_ld_wait(dp);
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const int col = 32 * h + c;
+            const float4 nd = rb4[16 + (col >> 2)];  // -D
+            const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
+            const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
+                                     fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                           make_float2(nd.x, nd.y)));
+            const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
+                                     fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                                           make_float2(nd.z, nd.w)));
+            dsk[c >> 1] = pack_bf16x2(d01.x, d01.y);
+            dsk[(c >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pkh[i] = pk[16 * h + i];
+          tmem_st16(t_dp + 32 * h, pkh);       // P^T of these queries
+          tmem_st16(t_dp + 32 * h + 16, dsk);  // dS^T of these queries
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars.ds_half[h]);
+        }
+      }
+      // Epilogue: warpgroup 0 stages dV in the dO ring slot of the tile's last
+      // block, warpgroup 1 stages scale * dK in its Q ring slot; the producer
+      // warp stores them. The accumulators may be overwritten by the next
+      // tile's first products only after this thread's next ds_half arrival.
+      const int g_last = g - 1;
+      bool done = ok && mbar_wait(&bars.kv_done, k & 1, abort_flag);
+      done = __all_sync(0xffffffffu, done);
+      if (done) {
+        tc_fence_after();
+        uint8_t* stage = w == 0 ? smem + C::kOffDO + (g_last % C::kDOStages) * C::kTileBytes
+                                : smem + C::kOffQ + (g_last % C::kQStages) * C::kTileBytes;
         stage_row_bf16<D>(tmem + lane_off + (w == 0 ? C::kColDV : C::kColDK), stage, r, 0, w == 0 ? 1.f : a.scale);
         fence_proxy_async_smem();
       }
-      named_bar_sync(1 + w, 128);
-      if (tt == 0 && !*abort_flag) {
-        for (int pn = 0; pn < D / 64; ++pn)
-          tma_store_3d(w == 0 ? &a.tm_dv : &a.tm_dk, stage + pn * kPanelBytes, pn * 64, kblk * C::BK, bh);
-        bulk_commit();
-        bulk_wait0();
-      }
+      tc_fence_before();
+      mbar_arrive(&bars.ep_staged[k & 7]);
+      ok = ok && done;
+      // the group's warps agree on going on (they read the same tile ring slot)
+      if (!named_bar_and(1 + w, 128, L_next >= 0)) break;
+      L = L_next;
+      t = nt;
     }
   }
 
@@ -1025,14 +1204,14 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  kv<<<dim3((unsigned)a.BH, nblk), 320, DkdvCfg<D>::kSmemBytes, stream>>>(a);
+  // persistent: one CTA per SM at most (both main kernels take their tiles from counters)
+  const long long tiles = (long long)a.BH * nblk;
+  kv<<<(unsigned)std::min<long long>(tiles, num_sms), 320, DkdvCfg<D>::kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kq = fa_bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  // persistent: one CTA per SM at most (the dQ tiles are handed out by a counter)
-  const long long tiles = (long long)a.BH * nblk;
   kq<<<(unsigned)std::min<long long>(tiles, num_sms), 320, DqCfg<D>::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
