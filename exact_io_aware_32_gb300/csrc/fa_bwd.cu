@@ -91,11 +91,12 @@ struct DkdvCfg {
   static constexpr int BK = 128;  // keys per tile
   static constexpr int BQ = 128;  // queries per iteration
   static constexpr int kTileBytes = (D / 64) * kPanelBytes;
-  // Q is needed first in each block (by S^T) and dO later (by dP^T and dV), so
-  // Q gets the deeper ring: its load for block i+2 starts when dK of block i-1
-  // completes.
+  // Q is needed first in each block (by S^T, two blocks ahead) and dO later
+  // (by dP^T, one block ahead), so Q gets the deeper ring. Both slots of block
+  // i are released together once its dV completes.
   static constexpr int kQStages = D == 128 ? 3 : 4;
   static constexpr int kDOStages = D == 128 ? 2 : 4;
+  static_assert(kDOStages <= kQStages && kQStages <= 4, "the slot-release ring is indexed by Q slot");
   static constexpr int kItemSlots = 4;  // tiles fetched ahead by the producer
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
@@ -115,7 +116,10 @@ struct DkdvCfg {
 struct DkdvBarriers {
   uint64_t item_full[4], item_empty[4];     // tile ring: producer -> MMA warp and warpgroups
   uint64_t k_full, k_empty, v_full, v_empty;  // K and V buffers (one tile each)
-  uint64_t q_full[4], q_empty[4], do_full[4], do_empty[4];
+  uint64_t q_full[4], do_full[4];
+  // block b's Q and dO slots are free again: barrier b % kQStages, phase b / kQStages
+  // (one commit after its dV; the producer arrives instead for a tile's last block)
+  uint64_t blk_free[4];
   uint64_t s_full, s_free, dp_full, ds_half[2];
   uint64_t kv_done, teardown;  // a tile's dV, dK complete
   // tile j's dV, dK staged in its last ring slots: barrier j % 8, phase j / 8. The
@@ -123,6 +127,7 @@ struct DkdvBarriers {
   // by parity would be ambiguous.
   uint64_t ep_staged[8];
   int item[4];
+  int st_bh[8], st_kblk[8], st_last[8];  // producer: tiles by k % 8 (head, key block, last block)
   uint32_t tmem_base;
   int abort;
 };
@@ -183,12 +188,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     mbar_init(&bars.v_empty, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&bars.q_full[s], 1);
-      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.blk_free[s], 1);
     }
-    for (int s = 0; s < C::kDOStages; ++s) {
-      mbar_init(&bars.do_full[s], 1);
-      mbar_init(&bars.do_empty[s], 1);
-    }
+    for (int s = 0; s < C::kDOStages; ++s) mbar_init(&bars.do_full[s], 1);
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.s_free, 256);
     mbar_init(&bars.dp_full, 1);
@@ -240,23 +242,21 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       tma_prefetch_desc(&a.tm_v);
     }
     __syncwarp();
-    DkdvTile hist[8];  // recent tiles (by k & 7) and the global index of their last block
-    int hist_last[8];
     int g = 0, ntiles = 0, next_store = 0;
+    int due = INT_MAX;  // last block of tile next_store, once that tile is known
     int q_issued = 0, do_issued = 0, kv_tiles = 0;
     bool ok = true;
     // store tile j's staged dV (dO slot of its last block) and dK (Q slot)
     auto store_tile = [&](int j, bool last) -> bool {
       if (!warp_wait(&bars.ep_staged[j & 7], (j >> 3) & 1, abort_flag)) return false;
       if (elect_one()) {
-        const DkdvTile tj = hist[j & 7];
-        const int gl = hist_last[j & 7];
+        const int bh = bars.st_bh[j & 7], kblk = bars.st_kblk[j & 7], gl = bars.st_last[j & 7];
         uint8_t* dv_stage = smem + C::kOffDO + (gl % C::kDOStages) * C::kTileBytes;
         uint8_t* dk_stage = smem + C::kOffQ + (gl % C::kQStages) * C::kTileBytes;
         if (!*abort_flag) {
           for (int pn = 0; pn < D / 64; ++pn) {
-            tma_store_3d(&a.tm_dv, dv_stage + pn * kPanelBytes, pn * 64, tj.kblk * C::BK, tj.bh);
-            tma_store_3d(&a.tm_dk, dk_stage + pn * kPanelBytes, pn * 64, tj.kblk * C::BK, tj.bh);
+            tma_store_3d(&a.tm_dv, dv_stage + pn * kPanelBytes, pn * 64, kblk * C::BK, bh);
+            tma_store_3d(&a.tm_dk, dk_stage + pn * kPanelBytes, pn * 64, kblk * C::BK, bh);
           }
           bulk_commit();
         }
@@ -264,17 +264,17 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           bulk_wait0();
         else
           bulk_wait_read0();
-        mbar_arrive(&bars.do_empty[gl % C::kDOStages]);  // in place of the MMA warp's release
-        mbar_arrive(&bars.q_empty[gl % C::kQStages]);
+        mbar_arrive(&bars.blk_free[gl % C::kQStages]);  // in place of the MMA warp's release
       }
       __syncwarp();
       return true;
     };
     // before block g reuses a slot of a ring with 'stages' slots
     auto store_due = [&](int g_next, int stages) -> bool {
-      while (next_store < ntiles && hist_last[next_store & 7] + stages <= g_next) {
+      while (due <= g_next - stages) {
         if (!store_tile(next_store, false)) return false;
         ++next_store;
+        due = next_store < ntiles ? bars.st_last[next_store & 7] : INT_MAX;
       }
       return true;
     };
@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
       if (L >= total) break;
       const DkdvTile t = dkdv_tile<CAUSAL>(L, a, nq);
-      hist[k & 7] = t;
-      hist_last[k & 7] = g + t.n - 1;
+      bars.st_bh[k & 7] = t.bh;  // every lane writes the same values
+      bars.st_kblk[k & 7] = t.kblk;
+      bars.st_last[k & 7] = g + t.n - 1;
+      if (next_store == k) due = g + t.n - 1;
       ntiles = k + 1;
       if (k >= 1 && !(ok = warp_wait(&bars.k_empty, (k - 1) & 1, abort_flag))) break;
       if (elect_one()) {
@@ -305,7 +307,8 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       for (int it = 0; it < t.n; ++it, ++g) {
         const int qs = g % C::kQStages, ds = g % C::kDOStages;
         if (!(ok = store_due(g, C::kQStages))) break;
-        if (!(ok = warp_wait(&bars.q_empty[qs], ((g / C::kQStages) & 1) ^ 1, abort_flag))) break;
+        // block g - kQStages used this Q slot (parity 1 of a fresh barrier passes at once)
+        if (!(ok = warp_wait(&bars.blk_free[qs], ((g / C::kQStages) & 1) ^ 1, abort_flag))) break;
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars.q_full[qs], C::kTileBytes);
           for (int pn = 0; pn < D / 64; ++pn)
@@ -325,7 +328,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
           __syncwarp();
         }
         if (!(ok = store_due(g, C::kDOStages))) break;
-        if (!(ok = warp_wait(&bars.do_empty[ds], ((g / C::kDOStages) & 1) ^ 1, abort_flag))) break;
+        // block g - kDOStages used this dO slot (kDOStages <= kQStages: its phase cannot be overtaken)
+        if (g >= C::kDOStages) {
+          const int b = g - C::kDOStages;
+          if (!(ok = warp_wait(&bars.blk_free[b % C::kQStages], (b / C::kQStages) & 1, abort_flag))) break;
+        }
         if (elect_one()) {
           mbar_arrive_expect_tx(&bars.do_full[ds], C::kTileBytes);
           for (int pn = 0; pn < D / 64; ++pn)
@@ -405,13 +412,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         __syncwarp();
         return true;
       };
-      // do_waited: the caller has already waited for this block's dO (a tile's first block also needs V)
-      auto issue_dp = [&](int g, bool first, bool last, int kt, bool do_waited) -> bool {  // dP^T = V dO_i^T
+      // dP^T of a tile's first block: it also waits for the tile's V. Other blocks'
+      // dP^T is issued with the previous block's second dV/dK half.
+      auto issue_dp_first = [&](int g, bool last, int kt) -> bool {  // dP^T = V dO_i^T
         const int s = g % C::kDOStages;
-        bool ok = first       ? warp_wait2(&bars.do_full[s], do_phase(g), &bars.v_full, kt & 1, abort_flag)
-                  : do_waited ? true
-                              : warp_wait(&bars.do_full[s], do_phase(g), abort_flag);
-        if (!ok) return false;
+        if (!warp_wait2(&bars.do_full[s], do_phase(g), &bars.v_full, kt & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t so = s * C::kTileBytes;
         if (elect_one()) {
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       Blk b0 = next_blk(), b1 = {0, 0, -1};
       bool ok = b0.n > 0;
       if (ok) {
-        ok = issue_s(0, true, b0.n == 1, b0.kt) && issue_dp(0, true, b0.n == 1, b0.kt, false);
+        ok = issue_s(0, true, b0.n == 1, b0.kt) && issue_dp_first(0, b0.n == 1, b0.kt);
         b1 = next_blk();
         if (ok && b1.it > 0) ok = issue_s(1, false, b1.it == b1.n - 1, b1.kt);
       }
@@ -446,8 +451,11 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         const int qs = g % C::kQStages, ds = g % C::kDOStages;
         const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
         const bool last = it == b0.n - 1;
-        // the second half's wait also covers dO of the next block of the tile, whose dP^T follows
+        // Within a tile the second half's wait also covers dO of block g+1, and
+        // dP^T of block g+1 goes out with that half's products (one elected
+        // issue: no commit round trip between them on the tensor pipe's path).
         const bool pair_do = !last;
+        const bool last1 = b1.it == b1.n - 1;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (h == 1 && pair_do)
@@ -464,26 +472,33 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
               mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
                      kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
             }
-            // dK is Q's last reader: its slot refills sooner (a tile's last slots
-            // are released by the producer once their staged dK, dV are stored)
-            if (h == 1 && !last) mma_commit(&bars.q_empty[qs]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // dV += P^T dO_i
               const int kk = dkdv_half_kstep(h, i);
               mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
                      kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
             }
-            if (h == 1) mma_commit(last ? &bars.kv_done : &bars.do_empty[ds]);
+            if (h == 1) {
+              // the block's Q and dO slots are free once dV is done (a tile's last
+              // slots are released by the producer once their staged dK, dV are stored)
+              mma_commit(last ? &bars.kv_done : &bars.blk_free[qs]);
+              if (pair_do) {  // dP^T = V dO_{g+1}^T overwrites P^T, dS^T of block g: it follows dK, dV
+                const uint32_t so1 = ((g + 1) % C::kDOStages) * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so1 >> 4), kIdKK, kk > 0);
+                mma_commit(&bars.dp_full);
+                if (last1) mma_commit(&bars.v_empty);  // the tile's last reader of V
+              }
+            }
           }
           __syncwarp();
         }
         if (!ok) break;
-        // block g+1: its dP^T (and its S^T first if it starts a tile); block g+2: its S^T unless it starts one
+        // a next tile's first block: its S^T, then its dP^T; block g+2: its S^T unless it starts a tile
         Blk b2 = {0, 0, -1};
         if (b1.n > 0) {
-          const bool first1 = b1.it == 0, last1 = b1.it == b1.n - 1;
-          if (first1 && !(ok = issue_s(g + 1, true, last1, b1.kt))) break;
-          if (!(ok = issue_dp(g + 1, first1, last1, b1.kt, pair_do))) break;
+          if (!pair_do && !(ok = issue_s(g + 1, true, last1, b1.kt) && issue_dp_first(g + 1, last1, b1.kt))) break;
           b2 = next_blk();
           if (b2.it > 0 && !(ok = issue_s(g + 2, false, b2.it == b2.n - 1, b2.kt))) break;
         }
@@ -503,13 +518,14 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     const uint32_t t_s = tmem + lane_off + C::kColS + 64 * w;
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;  // dP^T, then P^T | dS^T (bf16)
     const float sl2 = a.scale_log2;
-    // Threads 0-63 of the warpgroup fetch -lse (log2 units) of the group's 64
-    // queries of query block qb, threads 64-127 fetch -D; one block ahead,
-    // through registers.
+    // Threads 0-63 of the warpgroup fetch lse of the group's 64 queries of
+    // query block qb, threads 64-127 fetch D; one block ahead, through
+    // registers, and negated (lse also to log2 units) only when stored a block
+    // later, so that no thread waits for the load in between.
     auto fetch = [&](const DkdvTile& t, int qb) -> float {
       const int q = qb * C::BQ + 64 * w + (tt & 63);
-      if (tt < 64) return q < N ? -a.lse[(size_t)t.bh * N + q] * kLog2e : -INFINITY;  // 2^(x - inf) = 0 past N
-      return q < N ? -a.Dsum[(size_t)t.bh * N + q] : 0.f;
+      if (tt < 64) return q < N ? a.lse[(size_t)t.bh * N + q] : INFINITY;  // 2^(x - inf) = 0 past N
+      return q < N ? a.Dsum[(size_t)t.bh * N + q] : 0.f;
     };
     // After a failed wait a warp keeps going without work; at every block the
     // group's named barrier also ANDs the warps' states, so the four warps
@@ -528,7 +544,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       for (int it = 0; it < t.n; ++it, ++g) {
         const int q0 = (t.i_start + it) * C::BQ;
         float* rb = rowbuf + ((g & 1) * 2 + w) * 128;
-        rb[tt] = next;
+        rb[tt] = tt < 64 ? -next * kLog2e : -next;  // -lse (log2 units) | -D
         ok = named_bar_and(1 + w, 128, ok);
         if (it + 1 < t.n) {
           next = fetch(t, t.i_start + it + 1);
