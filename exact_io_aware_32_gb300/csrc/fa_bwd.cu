@@ -20,10 +20,12 @@
 // L2's atomic-add rate, about 1.1-1.4e12 fp32 adds/s, would otherwise bound
 // the pass).
 //
-// Warp roles in both main kernels (320 threads): warpgroups 0 and 1 (warps
-// 0-7) do the elementwise work, each on half of the block's columns (thread r
-// owns TMEM lane r); warp 8 issues TMA loads; warp 9 issues the tcgen05 MMAs
-// and owns the 512-column TMEM allocation. P^T and dS^T (dK/dV kernel) and dS
+// Warp roles in both main kernels: warpgroups 0 and 1 (warps 0-7) do the
+// elementwise work, each on half of the block's columns (thread r owns TMEM
+// lane r); warp 8 issues TMA loads; warp 9 issues the tcgen05 MMAs and owns the
+// 512-column TMEM allocation; warp 10 issues the products that share no TMEM
+// columns with warp 9's (S^T in the dK/dV kernel, dQ in the dQ kernel), so
+// both kernels run 352 threads. P^T and dS^T (dK/dV kernel) and dS
 // (dQ kernel) are written back into TMEM as bf16 over fp32 columns the
 // warpgroups have already read, and used from there as the A operand of the
 // next product. Each S or dP tile is released to the MMA warp as soon as the
@@ -121,7 +123,9 @@ struct DkdvBarriers {
   // (one commit after its dV; the producer arrives instead for a tile's last block)
   uint64_t blk_free[4];
   uint64_t s_full, s_free, dp_full, ds_half[2];
-  uint64_t kv_done, teardown;  // a tile's dV, dK complete
+  uint64_t kv_done, teardown, teardown_s;  // a tile's dV, dK complete; each MMA warp's last products
+  // dP^T of block b issued (barrier b % 4, phase b / 4): the S^T warp follows it
+  uint64_t dp_issued[4];
   // tile j's dV, dK staged in its last ring slots: barrier j % 8, phase j / 8. The
   // producer stores up to a ring's depth of tiles late, so one barrier waited on
   // by parity would be ambiguous.
@@ -159,7 +163,7 @@ __device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nq) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     bars.abort = 0;
     for (int s = 0; s < C::kItemSlots; ++s) {
       mbar_init(&bars.item_full[s], 1);
-      mbar_init(&bars.item_empty[s], 1 + 8);  // the MMA warp and the 8 warpgroup warps
+      mbar_init(&bars.item_empty[s], 2 + 8);  // the two MMA warps and the 8 warpgroup warps
     }
     mbar_init(&bars.k_full, 1);
     mbar_init(&bars.k_empty, 1);
@@ -198,7 +202,9 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
     mbar_init(&bars.ds_half[1], 256);
     mbar_init(&bars.kv_done, 1);
     for (int j = 0; j < 8; ++j) mbar_init(&bars.ep_staged[j], 256);
+    for (int j = 0; j < 4; ++j) mbar_init(&bars.dp_issued[j], 1);
     mbar_init(&bars.teardown, 1);
+    mbar_init(&bars.teardown_s, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -356,10 +362,15 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       mbar_wait_drain(&bars.q_full[i % C::kQStages], (i / C::kQStages) & 1);
     for (int i = max(0, do_issued - C::kDOStages); i < do_issued; ++i)
       mbar_wait_drain(&bars.do_full[i % C::kDOStages], (i / C::kDOStages) & 1);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp follows the schedule, so it stays converged and its
-    // operands warp-uniform; one elected lane issues each group of tcgen05 ops.
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each tcgen05 instruction holds its issuing warp about as long as an
+    // N = 128 product holds the pipe, so a single issuing warp, with its waits
+    // and bookkeeping on top, would leave the pipe idle. Warp 9 issues dK, dV
+    // and dP^T, which share TMEM columns and so stay in one thread's issue
+    // order; warp 10 issues S^T (columns of its own) once warp 9 has issued the
+    // dP^T before it. Each warp stays converged and its operands warp-uniform;
+    // one elected lane issues each group of tcgen05 ops.
     {
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both operands K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dV, dK: A from TMEM, B MN-major
@@ -374,8 +385,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
       auto q_phase = [&](int g) { return (uint32_t)((g / C::kQStages) & 1); };
       auto do_phase = [&](int g) { return (uint32_t)((g / C::kDOStages) & 1); };
       // Blocks in run order as (position in the tile, tile size, tile index in
-      // the run); n == 0 past the end of the run. The loop keeps blocks g and
-      // g+1 in registers and takes g+2 after dP^T of block g+1 is issued.
+      // the run); n == 0 past the end of the run. Each warp walks the run itself.
       struct Blk {
         int it, n, kt;
       };
@@ -394,120 +404,126 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dkdv_kernel(const __grid_consta
         cursor = Blk{0, dkdv_tile<CAUSAL>(L, a, nq).n, cursor.kt + 1};
         return cursor;
       };
-      auto issue_s = [&](int g, bool first, bool last, int kt) -> bool {  // S^T = K Q_i^T
-        const int s = g % C::kQStages;
-        bool ok = g == 0 ? warp_wait(&bars.q_full[s], q_phase(g), abort_flag)
-                         : warp_wait2(&bars.s_free, (g - 1) & 1, &bars.q_full[s], q_phase(g), abort_flag);
-        if (ok && first) ok = warp_wait(&bars.k_full, kt & 1, abort_flag);
-        if (!ok) return false;
-        tc_fence_after();
-        const uint32_t so = s * C::kTileBytes;
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
-          mma_commit(&bars.s_full);
-          if (last) mma_commit(&bars.k_empty);  // the tile's last reader of K
-        }
-        __syncwarp();
-        return true;
-      };
-      // dP^T of a tile's first block: it also waits for the tile's V. Other blocks'
-      // dP^T is issued with the previous block's second dV/dK half.
-      auto issue_dp_first = [&](int g, bool last, int kt) -> bool {  // dP^T = V dO_i^T
-        const int s = g % C::kDOStages;
-        if (!warp_wait2(&bars.do_full[s], do_phase(g), &bars.v_full, kt & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t so = s * C::kTileBytes;
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
-          mma_commit(&bars.dp_full);
-          if (last) mma_commit(&bars.v_empty);  // the tile's last reader of V
-        }
-        __syncwarp();
-        return true;
-      };
-      // Per query block i the critical chain is: the warpgroups' dS^T of block
-      // i -> dV and dK of block i -> dP^T of block i+1 (it overwrites the
-      // columns that hold P^T and dS^T of block i, so it must follow dK in
-      // issue order: the products of one thread execute in that order) -> dS^T
-      // of block i+1. dV and dK start on the first half of the queries while
-      // the warpgroups still work on the second, and S^T of block i+2 goes
-      // after dP^T of block i+1 so that it fills the pipe while the warpgroups
-      // compute dS^T instead of delaying dV and dK. A tile's first S^T waits
-      // until the previous tile's last block (its K buffer then has had a
-      // block's time to refill).
-      Blk b0 = next_blk(), b1 = {0, 0, -1};
-      bool ok = b0.n > 0;
-      if (ok) {
-        ok = issue_s(0, true, b0.n == 1, b0.kt) && issue_dp_first(0, b0.n == 1, b0.kt);
-        b1 = next_blk();
-        if (ok && b1.it > 0) ok = issue_s(1, false, b1.it == b1.n - 1, b1.kt);
-      }
-      for (int g = 0; ok && b0.n > 0; ++g) {
-        const int it = b0.it;
-        const int qs = g % C::kQStages, ds = g % C::kDOStages;
-        const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
-        const bool last = it == b0.n - 1;
-        // Within a tile the second half's wait also covers dO of block g+1, and
-        // dP^T of block g+1 goes out with that half's products (one elected
-        // issue: no commit round trip between them on the tensor pipe's path).
-        const bool pair_do = !last;
-        const bool last1 = b1.it == b1.n - 1;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h == 1 && pair_do)
-            ok = warp_wait2(&bars.ds_half[1], g & 1, &bars.do_full[(g + 1) % C::kDOStages], do_phase(g + 1),
-                            abort_flag);
+      if (warp == 10) {
+        // S^T = K Q_g^T of every block, after the warpgroups have read S^T of
+        // block g-1 and warp 9 has issued dP^T of block g-1: the pipe then runs
+        // it while the warpgroups compute dS^T of block g-1.
+        bool ok = true;
+        for (int g = 0; ok; ++g) {
+          const Blk b = next_blk();
+          if (b.n == 0) break;
+          const int s = g % C::kQStages;
+          if (g == 0)
+            ok = warp_wait(&bars.q_full[s], q_phase(g), abort_flag);
           else
-            ok = warp_wait(&bars.ds_half[h], g & 1, abort_flag);
+            ok = warp_wait2(&bars.s_free, (g - 1) & 1, &bars.q_full[s], q_phase(g), abort_flag) &&
+                 warp_wait(&bars.dp_issued[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag);
+          if (ok && b.it == 0) ok = warp_wait(&bars.k_full, b.kt & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
+          const uint32_t so = s * C::kTileBytes;
           if (elect_one()) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {  // dK += dS^T Q_i
-              const int kk = dkdv_half_kstep(h, i);
-              mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
-                     kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {  // dV += P^T dO_i
-              const int kk = dkdv_half_kstep(h, i);
-              mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
-                     kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (h == 1) {
-              // the block's Q and dO slots are free once dV is done (a tile's last
-              // slots are released by the producer once their staged dK, dV are stored)
-              mma_commit(last ? &bars.kv_done : &bars.blk_free[qs]);
-              if (pair_do) {  // dP^T = V dO_{g+1}^T overwrites P^T, dS^T of block g: it follows dK, dV
-                const uint32_t so1 = ((g + 1) % C::kDOStages) * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                  mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so1 >> 4), kIdKK, kk > 0);
-                mma_commit(&bars.dp_full);
-                if (last1) mma_commit(&bars.v_empty);  // the tile's last reader of V
-              }
-            }
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + C::kColS, dk0 + koff(kk), dq0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
+            mma_commit(&bars.s_full);
+            if (b.it == b.n - 1) mma_commit(&bars.k_empty);  // the tile's last reader of K
           }
           __syncwarp();
         }
-        if (!ok) break;
-        // a next tile's first block: its S^T, then its dP^T; block g+2: its S^T unless it starts a tile
-        Blk b2 = {0, 0, -1};
-        if (b1.n > 0) {
-          if (!pair_do && !(ok = issue_s(g + 1, true, last1, b1.kt) && issue_dp_first(g + 1, last1, b1.kt))) break;
-          b2 = next_blk();
-          if (b2.it > 0 && !(ok = issue_s(g + 2, false, b2.it == b2.n - 1, b2.kt))) break;
+        if (elect_one()) mma_commit(&bars.teardown_s);  // the same lane as above: elect.sync picks the lowest
+        __syncwarp();
+        mbar_wait_drain(&bars.teardown_s, 0);
+      } else {
+        // dP^T of a tile's first block: it also waits for the tile's V. Other
+        // blocks' dP^T is issued with the previous block's second dV/dK half.
+        auto issue_dp_first = [&](int g, bool last, int kt) -> bool {  // dP^T = V dO_i^T
+          const int s = g % C::kDOStages;
+          if (!warp_wait2(&bars.do_full[s], do_phase(g), &bars.v_full, kt & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t so = s * C::kTileBytes;
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so >> 4), kIdKK, kk > 0);
+            mma_commit(&bars.dp_full);
+            if (last) mma_commit(&bars.v_empty);  // the tile's last reader of V
+            mbar_arrive(&bars.dp_issued[g & 3]);
+          }
+          __syncwarp();
+          return true;
+        };
+        // Per query block i the critical chain is: the warpgroups' dS^T of
+        // block i -> dV and dK of block i -> dP^T of block i+1 (it overwrites
+        // the columns that hold P^T and dS^T of block i, so it must follow dK
+        // in issue order: the products of one thread execute in that order) ->
+        // dS^T of block i+1. dV and dK start on the first half of the queries
+        // while the warpgroups still work on the second.
+        Blk b0 = next_blk(), b1 = {0, 0, -1};
+        bool ok = b0.n > 0;
+        if (ok) {
+          ok = issue_dp_first(0, b0.n == 1, b0.kt);
+          b1 = next_blk();
         }
-        b0 = b1;
-        b1 = b2;
+        for (int g = 0; ok && b0.n > 0; ++g) {
+          const int it = b0.it;
+          const int qs = g % C::kQStages, ds = g % C::kDOStages;
+          const uint32_t qso = qs * C::kTileBytes, dso = ds * C::kTileBytes;
+          const bool last = it == b0.n - 1;
+          // Within a tile the second half's wait also covers dO of block g+1,
+          // and dP^T of block g+1 goes out with that half's products (one
+          // elected issue: no commit round trip between them).
+          const bool pair_do = !last;
+          const bool last1 = b1.it == b1.n - 1;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1 && pair_do)
+              ok = warp_wait2(&bars.ds_half[1], g & 1, &bars.do_full[(g + 1) % C::kDOStages], do_phase(g + 1),
+                              abort_flag);
+            else
+              ok = warp_wait(&bars.ds_half[h], g & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // dK += dS^T Q_i
+                const int kk = dkdv_half_kstep(h, i);
+                mma_ts(tmem + C::kColDK, tmem + C::kColDP + dkdv_pcol(kk, true), dqm0 + ((kk * 2048 + qso) >> 4),
+                       kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // dV += P^T dO_i
+                const int kk = dkdv_half_kstep(h, i);
+                mma_ts(tmem + C::kColDV, tmem + C::kColDP + dkdv_pcol(kk, false), ddom0 + ((kk * 2048 + dso) >> 4),
+                       kIdTS, (it > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (h == 1) {
+                // the block's Q and dO slots are free once dV is done (a tile's last
+                // slots are released by the producer once their staged dK, dV are stored)
+                mma_commit(last ? &bars.kv_done : &bars.blk_free[qs]);
+                if (pair_do) {  // dP^T = V dO_{g+1}^T overwrites P^T, dS^T of block g: it follows dK, dV
+                  const uint32_t so1 = ((g + 1) % C::kDOStages) * C::kTileBytes;
+#pragma unroll
+                  for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kColDP, dv0 + koff(kk), ddo0 + koff(kk) + (so1 >> 4), kIdKK, kk > 0);
+                  mma_commit(&bars.dp_full);
+                  if (last1) mma_commit(&bars.v_empty);  // the tile's last reader of V
+                  mbar_arrive(&bars.dp_issued[(g + 1) & 3]);
+                }
+              }
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          // a next tile's first block: its dP^T (its S^T comes from warp 10)
+          if (b1.n > 0 && !pair_do && !(ok = issue_dp_first(g + 1, last1, b1.kt))) break;
+          b0 = b1;
+          b1 = b1.n > 0 ? next_blk() : Blk{0, 0, -1};
+        }
+        if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
+        __syncwarp();
+        mbar_wait_drain(&bars.teardown, 0);
       }
-      if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
-      __syncwarp();
-      mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
@@ -701,12 +717,13 @@ struct DqBarriers {
   uint64_t q_full, qt_ready;             // Q buffer (one tile) loaded; Q copied into TMEM
   uint64_t do_full, do_empty;            // dO buffer (one tile)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_tile, teardown;
+  uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_tile, teardown, teardown_q;
   uint64_t ep_staged, dq_stored;        // dQ of a tile staged in the Q buffer; its store has read it
   int item[4];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(DqBarriers) <= 512, "dQ barriers exceed their shared memory");
 
 // Copies row r (D bf16) of a 128-row, 128-byte-swizzled tile into TMEM as D / 2
 // columns of bf16 pairs at taddr (this thread's lane).
@@ -743,7 +760,7 @@ __device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -759,7 +776,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     bars.abort = 0;
     for (int s = 0; s < C::kItemSlots; ++s) {
       mbar_init(&bars.item_full[s], 1);
-      mbar_init(&bars.item_empty[s], 1 + 8);  // the MMA warp and the 8 warpgroup warps
+      mbar_init(&bars.item_empty[s], 2 + 8);  // the two MMA warps and the 8 warpgroup warps
     }
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.qt_ready, 256);
@@ -782,6 +799,7 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(&bars.ep_staged, 256);
     mbar_init(&bars.dq_stored, 1);
     mbar_init(&bars.teardown, 1);
+    mbar_init(&bars.teardown_q, 1);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -914,9 +932,14 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
     for (int i = max(0, v_issued - C::kVStages); i < v_issued; ++i)
       mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // Whole warp, converged; one elected lane issues (as in the dK/dV kernel).
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two warps share the issue (a tcgen05 instruction holds its warp about as
+    // long as an N = 128 product holds the pipe): warp 9 issues S and dP of the
+    // next block as soon as the warpgroups have read the current one, warp 10
+    // issues dQ += dS K as soon as dS is in TMEM. Their products use disjoint
+    // TMEM columns; every hand-over goes through an mbarrier. Each warp stays
+    // converged; one elected lane issues each group of tcgen05 ops.
     {
       constexpr uint32_t kIdKK = idesc_bf16(128, 128, false, false);  // S (A from TMEM), dP: B K-major
       constexpr uint32_t kIdTS = idesc_bf16(128, D, false, true);     // dQ: dS from TMEM, K MN-major
@@ -927,89 +950,102 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       auto koff = [](int kk) -> uint32_t { return ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4; };
       auto k_phase = [&](int g) { return (uint32_t)((g / C::kKStages) & 1); };
       auto v_phase = [&](int g) { return (uint32_t)((g / C::kVStages) & 1); };
-      // The issue_* helpers expect their operands' barriers to have been waited on.
-      auto issue_s = [&](int g) {  // S = Q K_g^T
-        const int sk = g % C::kKStages;
-        tc_fence_after();
-        const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(tmem + C::kColS, tmem + C::kColQ + 8 * kk, dk0 + koff(kk) + ko, kIdKK, kk > 0);
-          mma_commit(&bars.s_full);
-        }
-        __syncwarp();
-      };
-      auto issue_dp = [&](int g, bool last_of_tile) {  // dP = dO V_g^T
-        const int sv = g % C::kVStages;
-        tc_fence_after();
-        const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
-          mma_commit(&bars.dp_full);
-          mma_commit(&bars.v_empty[sv]);
-          if (last_of_tile) mma_commit(&bars.do_empty);  // the tile's last reader of dO
-        }
-        __syncwarp();
-      };
-      int k = 0, g = 0;  // tile and key block over the CTA's run
-      int L = take_tile(0);
-      DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
-      bool ok = L >= 0;
-      if (ok) {  // the first tile's first block
-        ok = warp_wait2(&bars.qt_ready, 0, &bars.k_full[0], 0, abort_flag);
-        if (ok) issue_s(0);
-        ok = ok && warp_wait2(&bars.do_full, 0, &bars.v_full[0], 0, abort_flag);
-        if (ok) issue_dp(0, t.nk == 1);
-      }
-      while (ok) {
-        for (int j = 0; ok && j < t.nk; ++j) {
-          const int gj = g + j;
-          if (j + 1 < t.nk) {  // next block of this tile
-            if (!(ok = warp_wait2(&bars.s_free, gj & 1, &bars.k_full[(gj + 1) % C::kKStages], k_phase(gj + 1),
-                                  abort_flag)))
+      if (warp == 10) {
+        // dQ += dS K_j of every key block j, once the warpgroups have written dS;
+        // the product is K's last reader.
+        int k = 0, g = 0;  // tile and key block over the CTA's run
+        bool ok = true;
+        for (int L = take_tile(0); ok && L >= 0; L = take_tile(++k)) {
+          const DqTile t = dq_tile<CAUSAL>(L, a, nq);
+          for (int j = 0; j < t.nk; ++j) {
+            const int gj = g + j;
+            if (!(ok = warp_wait2(&bars.ds_ready, gj & 1, &bars.k_full[gj % C::kKStages], k_phase(gj), abort_flag)))
               break;
-            issue_s(gj + 1);
-            if (!(ok = warp_wait2(&bars.dp_free, gj & 1, &bars.v_full[(gj + 1) % C::kVStages], v_phase(gj + 1),
-                                  abort_flag)))
-              break;
-            issue_dp(gj + 1, j + 1 == t.nk - 1);
+            tc_fence_after();
+            const uint32_t ko = (uint32_t)((gj % C::kKStages) * C::kTileBytes);
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
+                mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
+                       dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(&bars.k_empty[gj % C::kKStages]);
+              if (j == t.nk - 1) mma_commit(&bars.dq_tile);
+            }
+            __syncwarp();
           }
-          if (!(ok = warp_wait(&bars.ds_ready, gj & 1, abort_flag))) break;
+          g += t.nk;
+        }
+        if (elect_one()) mma_commit(&bars.teardown_q);  // the same lane as above: elect.sync picks the lowest
+        __syncwarp();
+        mbar_wait_drain(&bars.teardown_q, 0);
+      } else {
+        // S and dP of each key block, once the warpgroups hold the previous
+        // block's S (resp. dP) in registers and the operands are loaded.
+        auto issue_s = [&](int g) {  // S = Q K_g^T
+          const int sk = g % C::kKStages;
           tc_fence_after();
-          const uint32_t ko = (uint32_t)((gj % C::kKStages) * C::kTileBytes);
+          const uint32_t ko = (uint32_t)(sk * C::kTileBytes) >> 4;
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K_j  (K = 128 keys)
-              mma_ts(tmem + C::kColDQ, tmem + C::kColDS + 32 * (kk >> 2) + 8 * (kk & 3),
-                     dkm0 + ((kk * 2048 + ko) >> 4), kIdTS, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars.k_empty[gj % C::kKStages]);
-            if (j == t.nk - 1) mma_commit(&bars.dq_tile);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ts(tmem + C::kColS, tmem + C::kColQ + 8 * kk, dk0 + koff(kk) + ko, kIdKK, kk > 0);
+            mma_commit(&bars.s_full);
           }
           __syncwarp();
+        };
+        auto issue_dp = [&](int g, bool last_of_tile) {  // dP = dO V_g^T
+          const int sv = g % C::kVStages;
+          tc_fence_after();
+          const uint32_t vo = (uint32_t)(sv * C::kTileBytes) >> 4;
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + C::kColDP, ddo0 + koff(kk), dv0 + koff(kk) + vo, kIdKK, kk > 0);
+            mma_commit(&bars.dp_full);
+            mma_commit(&bars.v_empty[sv]);
+            if (last_of_tile) mma_commit(&bars.do_empty);  // the tile's last reader of dO
+          }
+          __syncwarp();
+        };
+        int k = 0, g = 0;  // tile and key block over the CTA's run
+        int L = take_tile(0);
+        DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
+        bool ok = L >= 0;
+        while (ok) {
+          // the tile's first block: S needs its Q in TMEM (the warpgroups copy it
+          // after the previous tile's last S has been read), dP its dO (loaded
+          // once the previous tile's last dP has read the buffer)
+          if (!(ok = (g == 0 ? warp_wait(&bars.qt_ready, k & 1, abort_flag)
+                             : warp_wait2(&bars.s_free, (g - 1) & 1, &bars.qt_ready, k & 1, abort_flag)) &&
+                     warp_wait(&bars.k_full[g % C::kKStages], k_phase(g), abort_flag)))
+            break;
+          issue_s(g);
+          if (!(ok = (g == 0 ? warp_wait(&bars.do_full, k & 1, abort_flag)
+                             : warp_wait2(&bars.dp_free, (g - 1) & 1, &bars.do_full, k & 1, abort_flag)) &&
+                     warp_wait(&bars.v_full[g % C::kVStages], v_phase(g), abort_flag)))
+            break;
+          issue_dp(g, t.nk == 1);
+          for (int j = 1; j < t.nk; ++j) {
+            const int gj = g + j;
+            if (!(ok = warp_wait2(&bars.s_free, (gj - 1) & 1, &bars.k_full[gj % C::kKStages], k_phase(gj),
+                                  abort_flag)))
+              break;
+            issue_s(gj);
+            if (!(ok = warp_wait2(&bars.dp_free, (gj - 1) & 1, &bars.v_full[gj % C::kVStages], v_phase(gj),
+                                  abort_flag)))
+              break;
+            issue_dp(gj, j == t.nk - 1);
+          }
+          if (!ok) break;
+          g += t.nk;
+          ++k;
+          if ((L = take_tile(k)) < 0) break;
+          t = dq_tile<CAUSAL>(L, a, nq);
         }
-        if (!ok) break;
-        // The next tile's first block: S needs its Q in TMEM (the warpgroups copy
-        // it after this tile's last block), dP its dO (loaded once this tile's
-        // last dP has read the buffer).
-        g += t.nk;
-        ++k;
-        if ((L = take_tile(k)) < 0) break;
-        t = dq_tile<CAUSAL>(L, a, nq);
-        if (!(ok = warp_wait2(&bars.s_free, (g - 1) & 1, &bars.qt_ready, k & 1, abort_flag) &&
-                   warp_wait(&bars.k_full[g % C::kKStages], k_phase(g), abort_flag)))
-          break;
-        issue_s(g);
-        if (!(ok = warp_wait2(&bars.dp_free, (g - 1) & 1, &bars.do_full, k & 1, abort_flag) &&
-                   warp_wait(&bars.v_full[g % C::kVStages], v_phase(g), abort_flag)))
-          break;
-        issue_dp(g, t.nk == 1);
+        if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
+        __syncwarp();
+        mbar_wait_drain(&bars.teardown, 0);
       }
-      if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
-      __syncwarp();
-      mbar_wait_drain(&bars.teardown, 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
@@ -1144,7 +1180,6 @@ __global__ void __launch_bounds__(320, 1) fa_bwd_dq_kernel(const __grid_constant
       // so that its first S runs while this tile's dQ is written out; its row
       // terms are loaded here and converted when it starts.
       g += t.nk;
-      const DqTile cur = t;
       L = take_tile(k + 1);
       DqTile nt = {0, 0, 0};
       float lse_next = 0.f, d_next = 0.f;
@@ -1222,13 +1257,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
     return e;
   // persistent: one CTA per SM at most (both main kernels take their tiles from counters)
   const long long tiles = (long long)a.BH * nblk;
-  kv<<<(unsigned)std::min<long long>(tiles, num_sms), 320, DkdvCfg<D>::kSmemBytes, stream>>>(a);
+  kv<<<(unsigned)std::min<long long>(tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kq = fa_bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  kq<<<(unsigned)std::min<long long>(tiles, num_sms), 320, DqCfg<D>::kSmemBytes, stream>>>(a);
+  kq<<<(unsigned)std::min<long long>(tiles, num_sms), 352, DqCfg<D>::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 
