@@ -42,11 +42,15 @@ struct FwdCfg {
   static constexpr int kPanels = D / 64;         // 128-byte-wide column panels per row
   static constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int kTileBytes = kPanels * kPanelBytes;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  // K of a block is released once both tiles' S have read it, V only once both
+  // PV products have: V gets the deeper ring, so its load has more than one
+  // block's time to land.
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = D == 128 ? 3 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
   // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 reuses its first 64)
   // and O_t (fp32, D columns) for query tiles t = 0, 1.
@@ -90,9 +94,11 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     bars.abort = 0;
     mbar_init(&bars.q_full[0], 1);
     mbar_init(&bars.q_full[1], 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
@@ -137,14 +143,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     bool q1_issued = false;
     int nk_issued = 0, nv_issued = 0;
     for (int j = 0; j < nb_max; ++j) {
-      const int s = j % C::kStages;
-      const uint32_t ph = (j / C::kStages) & 1;
-      if (!warp_wait(&bars.k_empty[s], ph ^ 1, abort_flag)) break;
+      const int sk = j % C::kKStages, sv = j % C::kVStages;
+      if (!warp_wait(&bars.k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+        mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[s], pn * 64,
-                      j * C::BN, bh);
+          tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[sk],
+                      pn * 64, j * C::BN, bh);
       }
       __syncwarp();
       nk_issued = j + 1;
@@ -152,12 +157,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         load_q(1);
         q1_issued = true;
       }
-      if (!warp_wait(&bars.v_empty[s], ph ^ 1, abort_flag)) break;
+      if (!warp_wait(&bars.v_empty[sv], ((j / C::kVStages) & 1) ^ 1, abort_flag)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+        mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[s], pn * 64,
-                      j * C::BN, bh);
+          tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[sv],
+                      pn * 64, j * C::BN, bh);
       }
       __syncwarp();
       nv_issued = j + 1;
@@ -165,10 +170,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // Let every issued copy land before the CTA can exit.
     mbar_wait_drain(&bars.q_full[0], 0);
     if (q1_issued) mbar_wait_drain(&bars.q_full[1], 0);
-    for (int i = max(0, nk_issued - C::kStages); i < nk_issued; ++i)
-      mbar_wait_drain(&bars.k_full[i % C::kStages], (i / C::kStages) & 1);
-    for (int i = max(0, nv_issued - C::kStages); i < nv_issued; ++i)
-      mbar_wait_drain(&bars.v_full[i % C::kStages], (i / C::kStages) & 1);
+    for (int i = max(0, nk_issued - C::kKStages); i < nk_issued; ++i)
+      mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
+    for (int i = max(0, nv_issued - C::kVStages); i < nv_issued; ++i)
+      mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp follows the schedule, so it stays converged and its
@@ -216,8 +221,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       // before S_t(j + 1) writes them, and when S_t(j + 1) completes, so has
       // PV_t(j) (the softmax may then rescale O_t).
       for (int j = 0; ok && j < nb_max; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
+        const int s = j % C::kVStages;
+        const uint32_t ph = (j / C::kVStages) & 1;
+        const int v_last = j < nb[1] ? 1 : 0;  // the tile whose PV reads V_j last
         // V of this block is paired with tile 0's P (each mbarrier probe costs
         // about a hundred cycles; warp_wait2 overlaps the two)
         if (j < nb[0])
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         else
           ok = warp_wait(&bars.v_full[s], ph, abort_flag);
         if (!ok) break;
-        const int jn = j + 1, sn = jn % C::kStages;
+        const int jn = j + 1, sn = jn % C::kKStages;
         bool k_next = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < nb[t]) {
@@ -241,12 +247,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
               // only the epilogue waits for O (the softmax learns of earlier PV products through
               // the S products issued after them), so only the last one is committed
               if (j == nb[t] - 1) mma_commit(&bars.o_done[t]);
+              if (t == v_last) mma_commit(&bars.v_empty[s]);  // before the next S: V_j's slot refills sooner
             }
             __syncwarp();
           }
           if (jn < nb[t]) {
             if (!k_next) {
-              if (!(ok = warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, abort_flag))) break;
+              if (!(ok = warp_wait(&bars.k_full[sn], (jn / C::kKStages) & 1, abort_flag))) break;
               tc_fence_after();
               k_next = true;
             }
@@ -255,11 +262,10 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
           }
         }
         if (!ok) break;
-        if (elect_one()) {
-          mma_commit(&bars.v_empty[s]);
-          if (k_next) mma_commit(&bars.k_empty[sn]);
+        if (k_next) {
+          if (elect_one()) mma_commit(&bars.k_empty[sn]);
+          __syncwarp();
         }
-        __syncwarp();
       }
       if (elect_one()) mma_commit(&bars.teardown);
       __syncwarp();
