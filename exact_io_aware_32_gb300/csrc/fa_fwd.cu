@@ -224,15 +224,14 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         const int s = j % C::kVStages;
         const uint32_t ph = (j / C::kVStages) & 1;
         const int v_last = j < nb[1] ? 1 : 0;  // the tile whose PV reads V_j last
-        // V of this block is paired with tile 0's P (each mbarrier probe costs
-        // about a hundred cycles; warp_wait2 overlaps the two)
-        if (j < nb[0])
-          ok = warp_wait2(&bars.v_full[s], ph, &bars.p_full[0], j & 1, abort_flag);
-        else
-          ok = warp_wait(&bars.v_full[s], ph, abort_flag);
-        if (!ok) break;
         const int jn = j + 1, sn = jn % C::kKStages;
-        bool k_next = false;
+        const bool k_next = jn < nb_max;  // some tile reads K of the next block
+        // V of this block, tile 0's P and the next block's K (loaded two blocks
+        // ahead, so nearly always there) in one wait: each mbarrier probe costs
+        // about a hundred cycles, and the three overlap.
+        ok = warp_wait3(&bars.v_full[s], ph, j < nb[0] ? &bars.p_full[0] : &bars.v_full[s], j < nb[0] ? (j & 1) : ph,
+                        k_next ? &bars.k_full[sn] : &bars.v_full[s], k_next ? (jn / C::kKStages) & 1 : ph, abort_flag);
+        if (!ok) break;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < nb[t]) {
             if (t == 1 && !(ok = warp_wait(&bars.p_full[t], j & 1, abort_flag))) break;
@@ -252,11 +251,6 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             __syncwarp();
           }
           if (jn < nb[t]) {
-            if (!k_next) {
-              if (!(ok = warp_wait(&bars.k_full[sn], (jn / C::kKStages) & 1, abort_flag))) break;
-              tc_fence_after();
-              k_next = true;
-            }
             if (elect_one()) issue_s(t, sn);
             __syncwarp();
           }
@@ -382,7 +376,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_store_3d(&a.tm_o, stage + pn * C::kPanelBytes, pn * 64, qblk * 256 + t * 128, bh);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();  // the staging tile has been read; the writes finish on their own
       }
       if (ok && row < N) a.lse[(size_t)bh * N + row] = (m_ref + log2f(l_sum)) * kLn2;
     }

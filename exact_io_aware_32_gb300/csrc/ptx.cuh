@@ -87,6 +87,16 @@ __device__ __forceinline__ bool warp_wait2(uint64_t* bar0, uint32_t parity0, uin
   return warp_wait(bar0, parity0, abort) && warp_wait(bar1, parity1, abort);
 }
 
+// warp_wait on three barriers, the three probes in flight together.
+__device__ __forceinline__ bool warp_wait3(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                           uint64_t* bar2, uint32_t parity2, volatile int* abort) {
+  const bool done0 = mbar_try_wait(bar0, parity0);
+  const bool done1 = mbar_try_wait(bar1, parity1);
+  const bool done2 = mbar_try_wait(bar2, parity2);
+  if (__all_sync(0xffffffffu, done0 && done1 && done2)) return true;
+  return warp_wait(bar0, parity0, abort) && warp_wait(bar1, parity1, abort) && warp_wait(bar2, parity2, abort);
+}
+
 // Teardown wait used to let in-flight copies or MMAs finish before a CTA
 // exits: ignores the abort flag, still bounded by kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
