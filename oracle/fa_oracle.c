@@ -16,6 +16,14 @@
  * (the pages name a fused "mask" without defining it; the causal reading
  * j <= i is the plainest one and makes row 0 attend to key 0 only).
  *
+ * oracle_fwd_kv is the same forward with Nq query rows against Nk keys
+ * (q, o: [BH][Nq][d]; k, v: [BH][Nk][d]; lse: [BH][Nq]). Causal then aligns
+ * the queries with the last Nq keys: row i attends to {0..i + Nk - Nq}, so
+ * that the last row sees every key, as a decoding step does (the pages list
+ * unequal lengths and decode-style attention without defining their mask;
+ * this is the reading under which Nq = Nk gives the mask above). Causal needs
+ * Nq <= Nk, so that every row sees at least one key.
+ *
  * Forward, per head and row i (chapter 08 defines the row max m and the sum
  * of exponentials l that the tiled method carries; here they are taken over
  * the whole row at once):
@@ -50,6 +58,9 @@ static double dot(const double* a, const double* b, int d) {
 
 static int row_len(int i, int N, int causal) { return causal ? i + 1 : N; }
 
+/* Keys visible to query row i of Nq against Nk keys. */
+static int row_len_kv(int i, int Nq, int Nk, int causal) { return causal ? i + 1 + (Nk - Nq) : Nk; }
+
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -73,22 +84,24 @@ static void score_row(const double* qi, const double* k, int n, int d, double sc
 }
 
 /*
- * Forward pass. rows == NULL computes every row; otherwise only the nrows
- * listed rows of every head are written (o rows and lse entries elsewhere are
- * left untouched). Returns 0, or -1 on a bad argument or allocation failure.
+ * Forward pass, Nq query rows against Nk keys. rows == NULL computes every
+ * row; otherwise only the nrows listed rows of every head are written (o rows
+ * and lse entries elsewhere are left untouched). Returns 0, or -1 on a bad
+ * argument (including causal with Nq > Nk) or allocation failure.
  */
-int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int N, int d,
-               double scale, int causal, const int* rows, int nrows, int nthreads) {
-  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
-  if (!rows) nrows = N;
+int oracle_fwd_kv(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int Nq, int Nk,
+                  int d, double scale, int causal, const int* rows, int nrows, int nthreads) {
+  if (BH < 1 || Nq < 1 || Nk < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
+  if (causal && Nq > Nk) return -1;
+  if (!rows) nrows = Nq;
   for (int r = 0; rows && r < nrows; ++r)
-    if (rows[r] < 0 || rows[r] >= N) return -1;
+    if (rows[r] < 0 || rows[r] >= Nq) return -1;
   set_threads(nthreads);
   int failed = 0;
   const long long total = (long long)BH * nrows;
 #pragma omp parallel
   {
-    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
     if (!s) {
 #pragma omp atomic write
       failed = 1;
@@ -98,23 +111,30 @@ int oracle_fwd(const double* q, const double* k, const double* v, double* o, dou
       if (!s) continue;
       const int h = (int)(w / nrows);
       const int i = rows ? rows[w % nrows] : (int)(w % nrows);
-      const size_t hb = (size_t)h * N * d;
-      const double* qi = q + hb + (size_t)i * d;
-      const int n = row_len(i, N, causal);
+      const double* qi = q + ((size_t)h * Nq + i) * d;
+      const double* kh = k + (size_t)h * Nk * d;
+      const double* vh = v + (size_t)h * Nk * d;
+      const int n = row_len_kv(i, Nq, Nk, causal);
       double M, l;
-      score_row(qi, k + hb, n, d, scale, s, &M, &l);
-      double* oi = o + hb + (size_t)i * d;
+      score_row(qi, kh, n, d, scale, s, &M, &l);
+      double* oi = o + ((size_t)h * Nq + i) * d;
       for (int t = 0; t < d; ++t) oi[t] = 0.0;
       for (int j = 0; j < n; ++j) {
         const double p = exp(s[j] - M) / l;
-        const double* vj = v + hb + (size_t)j * d;
+        const double* vj = vh + (size_t)j * d;
         for (int t = 0; t < d; ++t) oi[t] += p * vj[t];
       }
-      lse[(size_t)h * N + i] = M + log(l);
+      lse[(size_t)h * Nq + i] = M + log(l);
     }
     free(s);
   }
   return failed ? -1 : 0;
+}
+
+/* Forward pass of self-attention (Nq = Nk = N): the listed rows, or all. */
+int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int N, int d,
+               double scale, int causal, const int* rows, int nrows, int nthreads) {
+  return oracle_fwd_kv(q, k, v, o, lse, BH, N, N, d, scale, causal, rows, nrows, nthreads);
 }
 
 /*

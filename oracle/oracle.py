@@ -18,7 +18,12 @@ Three independent views of the same definition live here:
   page's claim that the blocked result equals the whole-row softmax can be
   checked.
 
-Arrays are numpy float64 of shape [BH, N, d] (lse and D: [BH, N]).
+Arrays are numpy float64 of shape [BH, N, d] (lse and D: [BH, N]). The
+``*_kv`` functions take Nq query rows against Nk keys (q, o: [BH, Nq, d]; k, v:
+[BH, Nk, d]); causal then lets row i see keys 0 .. i + Nk - Nq, so the last
+row sees every key as in a decoding step, and ``merge_partials`` combines the
+results of disjoint key ranges with the logsumexp form of the chapter-08
+update rule.
 """
 from __future__ import annotations
 
@@ -61,6 +66,9 @@ def load(path: str | None = None):
         c_int, c_double = ctypes.c_int, ctypes.c_double
         lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, ip, c_int, c_int]
         lib.oracle_fwd.restype = c_int
+        lib.oracle_fwd_kv.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int, ip, c_int,
+                                      c_int]
+        lib.oracle_fwd_kv.restype = c_int
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int,
                                    ip, c_int, ip, c_int, c_int]
         lib.oracle_bwd.restype = c_int
@@ -116,6 +124,29 @@ def fwd(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=N
     return o, lse
 
 
+def fwd_kv(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None):
+    """O and lse for Nq query rows against Nk keys, fp64 (causal: row i sees keys <= i + Nk - Nq).
+
+    ``rows`` (optional) restricts the computation to those query rows of every
+    head; the other rows of the returned arrays are NaN.
+    """
+    lib = lib or load()
+    q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
+    BH, Nq, d = q3.shape
+    Nk = k3.shape[1]
+    if k3.shape != (BH, Nk, d) or v3.shape != (BH, Nk, d):
+        raise ValueError("k and v must be [BH, Nk, d] with q's BH and d")
+    o = np.full_like(q3, np.nan)
+    lse = np.full((BH, Nq), np.nan)
+    ridx, nr = _iptr(rows)
+    rc = lib.oracle_fwd_kv(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(o), _dptr(lse), BH, Nq, Nk, d, float(scale),
+                           int(causal), None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                           nr, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_fwd_kv failed (causal needs Nq <= Nk)")
+    return o, lse
+
+
 def bwd(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads: int = 0, lib=None):
     """dq, dk, dv and D (D_i = sum_j P_ij dP_ij) of L = sum(dO * O), fp64.
 
@@ -165,6 +196,41 @@ def materialised_fwd(q, k, v, scale: float, causal: bool):
     O = np.matmul(P, v3)
     lse = (M + np.log(ell))[..., 0]
     return O, lse, S, P
+
+
+def materialised_fwd_kv(q, k, v, scale: float, causal: bool):
+    """The standard computation for Nq query rows against Nk keys (tiny inputs only)."""
+    q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
+    Nq, Nk = q3.shape[1], k3.shape[1]
+    S = scale * np.matmul(q3, np.swapaxes(k3, 1, 2))
+    allowed = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        allowed = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    S = np.where(allowed[None], S, -np.inf)
+    M = S.max(axis=2, keepdims=True)
+    E = np.exp(S - M)
+    ell = E.sum(axis=2, keepdims=True)
+    O = np.matmul(E / ell, v3)
+    return O, (M + np.log(ell))[..., 0]
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine per-key-range results (each o normalised over its own range, with
+    its logsumexp) into the result over the union of the ranges.
+
+    With m = max_s lse_s and w_s = e^(lse_s - m): lse = m + ln sum_s w_s and
+    o = sum_s w_s o_s / sum_s w_s. This is the chapter-08 rule
+    l_new = e^(m - m_new) l + e^(m~ - m_new) l~ written for logsumexps
+    (lse = m + ln l), applied to all ranges at once. A range a row does not see
+    at all has lse_s = -inf and weight 0.
+    """
+    lse_s = np.asarray(lse_parts, dtype=np.float64)   # [S, ...]
+    o_s = np.asarray(o_parts, dtype=np.float64)       # [S, ..., d]
+    m = lse_s.max(axis=0)
+    w = np.where(np.isfinite(lse_s), np.exp(lse_s - m[None]), 0.0)
+    tot = w.sum(axis=0)
+    o = np.einsum("s...,s...d->...d", w, np.where(np.isfinite(lse_s)[..., None], o_s, 0.0)) / tot[..., None]
+    return o, m + np.log(tot)
 
 
 def materialised_bwd(q, k, v, dO, scale: float, causal: bool):

@@ -220,6 +220,79 @@ def pin_sampling(lib=None):
         assert np.array_equal(dv[:, [1, 39, 2]], dv2[:, [1, 39, 2]])
 
 
+# --------------------------------------------------------------------------
+# Nq query rows against Nk keys (causal: row i sees keys <= i + Nk - Nq).
+# --------------------------------------------------------------------------
+def _kv(seed, BH, Nq, Nk, d):
+    rng = np.random.default_rng(seed)
+    return _rand(rng, BH, Nq, d), _rand(rng, BH, Nk, d), _rand(rng, BH, Nk, d)
+
+
+def pin_kv_torch_sdpa(lib=None):
+    """O against torch's fp64 CPU scaled_dot_product_attention with the explicit bottom-right mask."""
+    for seed, (BH, Nq, Nk, d) in enumerate([(2, 1, 9, 4), (2, 5, 13, 8), (1, 13, 5, 8), (3, 7, 7, 16)]):
+        q, k, v = _kv(100 + seed, BH, Nq, Nk, d)
+        for causal in (False, True):
+            if causal and Nq > Nk:
+                continue
+            mask = None
+            if causal:
+                mask = torch.tensor(np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq))
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q), torch.tensor(k), torch.tensor(v), attn_mask=mask, scale=0.45).numpy()
+            o, lse = orc.fwd_kv(q, k, v, 0.45, causal, lib=lib)
+            assert np.allclose(o, ref, rtol=0, atol=1e-12), (Nq, Nk, causal)
+            S = 0.45 * np.einsum("bid,bjd->bij", q, k)
+            if causal:
+                S = np.where(mask.numpy()[None], S, -np.inf)
+            assert np.allclose(lse, torch.logsumexp(torch.tensor(S), dim=-1).numpy(), rtol=0, atol=1e-13)
+
+
+def pin_kv_suffix_of_self_attention(lib=None):
+    """Causal, Nq < Nk: the rows equal the last Nq rows of self-attention over Nk rows whose
+    first Nk - Nq query rows are anything (here random), and match the pinned self-attention oracle."""
+    BH, Nq, Nk, d = 2, 6, 17, 8
+    q, k, v = _kv(110, BH, Nq, Nk, d)
+    head = np.random.default_rng(111).standard_normal((BH, Nk - Nq, d))
+    o_full, lse_full = orc.fwd(np.concatenate([head, q], axis=1), k, v, 0.7, True, lib=lib)
+    o, lse = orc.fwd_kv(q, k, v, 0.7, True, lib=lib)
+    assert np.allclose(o, o_full[:, Nk - Nq:], rtol=0, atol=1e-14)
+    assert np.allclose(lse, lse_full[:, Nk - Nq:], rtol=0, atol=1e-14)
+
+
+def pin_kv_single_key_and_last_row(lib=None):
+    """Nk = 1: every row's output is v_0 and lse = scale q.k_0. Causal: the last row sees every
+    key, so it equals the unmasked row; Nq = Nk gives the self-attention result."""
+    q, k, v = _kv(120, 2, 4, 1, 5)
+    o, lse = orc.fwd_kv(q, k, v, 0.9, False, lib=lib)
+    assert np.allclose(o, np.broadcast_to(v, o.shape), rtol=0, atol=1e-15)
+    assert np.allclose(lse, 0.9 * np.einsum("bnd,bd->bn", q, k[:, 0]), rtol=0, atol=1e-14)
+    q, k, v = _kv(121, 2, 5, 23, 8)
+    oc, lc = orc.fwd_kv(q, k, v, 0.5, True, lib=lib)
+    on, ln = orc.fwd_kv(q, k, v, 0.5, False, lib=lib)
+    assert np.allclose(oc[:, -1], on[:, -1], rtol=0, atol=1e-14) and np.allclose(lc[:, -1], ln[:, -1], atol=1e-14)
+    assert not np.allclose(oc[:, 0], on[:, 0])
+    q, k, v = _kv(122, 2, 9, 9, 8)
+    for causal in (False, True):
+        o1, l1 = orc.fwd_kv(q, k, v, 0.5, causal, lib=lib)
+        o2, l2 = orc.fwd(q, k, v, 0.5, causal, lib=lib)
+        assert np.allclose(o1, o2, rtol=0, atol=1e-15) and np.allclose(l1, l2, rtol=0, atol=1e-15)
+
+
+def pin_kv_merge_of_key_ranges(lib=None):
+    """Results over disjoint key ranges, merged with the logsumexp rule, equal the result over all
+    keys; a range a row cannot see (lse = -inf) has no weight."""
+    BH, Nq, Nk, d = 2, 7, 30, 8
+    q, k, v = _kv(130, BH, Nq, Nk, d)
+    o, lse = orc.fwd_kv(q, k, v, 0.6, False, lib=lib)
+    parts = [orc.fwd_kv(q, k[:, a:b], v[:, a:b], 0.6, False, lib=lib) for a, b in ((0, 4), (4, 19), (19, 30))]
+    om, lm = orc.merge_partials([p[0] for p in parts], [p[1] for p in parts])
+    assert np.allclose(om, o, rtol=0, atol=1e-14) and np.allclose(lm, lse, rtol=0, atol=1e-13)
+    blank_o = np.full_like(parts[0][0], np.nan)
+    om2, lm2 = orc.merge_partials([p[0] for p in parts] + [blank_o], [p[1] for p in parts] + [np.full_like(lse, -np.inf)])
+    assert np.allclose(om2, o, rtol=0, atol=1e-14) and np.allclose(lm2, lse, rtol=0, atol=1e-13)
+
+
 ALL_PINS = [
     pin_zero_q_noncausal,
     pin_zero_q_causal,
@@ -234,4 +307,8 @@ ALL_PINS = [
     pin_gradient_identities,
     pin_zero_q_dv,
     pin_sampling,
+    pin_kv_torch_sdpa,
+    pin_kv_suffix_of_self_attention,
+    pin_kv_single_key_and_last_row,
+    pin_kv_merge_of_key_ranges,
 ]

@@ -15,9 +15,10 @@ SRC = os.path.join(os.path.dirname(orc.__file__), "fa_oracle.c")
 MUTANTS = [
     ("dropped_scale", "s[j] = scale * dot(qi, k + (size_t)j * d, d);", "s[j] = dot(qi, k + (size_t)j * d, d);"),
     ("causal_excludes_diagonal", "return causal ? i + 1 : N;", "return causal ? (i > 0 ? i : 1) : N;"),
-    ("lse_without_log_sum", "lse[(size_t)h * N + i] = M + log(l);", "lse[(size_t)h * N + i] = M;"),
-    ("output_reads_k_not_v", "const double* vj = v + hb + (size_t)j * d;\n        for (int t = 0; t < d; ++t) oi[t]",
-     "const double* vj = k + hb + (size_t)j * d;\n        for (int t = 0; t < d; ++t) oi[t]"),
+    ("lse_without_log_sum", "lse[(size_t)h * Nq + i] = M + log(l);", "lse[(size_t)h * Nq + i] = M;"),
+    ("output_reads_k_not_v", "const double* vh = v + (size_t)h * Nk * d;", "const double* vh = k + (size_t)h * Nk * d;"),
+    ("kv_causal_top_left", "return causal ? i + 1 + (Nk - Nq) : Nk;", "return causal ? i + 1 : Nk;"),
+    ("kv_query_head_stride", "const double* qi = q + ((size_t)h * Nq + i) * d;", "const double* qi = q + ((size_t)h * Nk + i) * d;"),
     ("D_wrong_sign", "Di += s[j] * dp[j];", "Di -= s[j] * dp[j];"),
     ("dq_dropped_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
     ("dk_transposed_operand", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
