@@ -101,27 +101,63 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, void* stream) {
+  return fa_fwd_kv(q, k, v, o, lse, B, H, N, N, d, scale, causal, nullptr, 0, stream);
+}
+
+size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_shape(B, H, Nq, d, 1.0f) != FA_OK || check_shape(B, H, Nk, d, 1.0f) != FA_OK) return 0;
+  DeviceInfo* di = nullptr;
+  if (device_info(&di) != FA_OK) return 0;
+  const int n = fa::pick_key_splits(B * H, Nq, Nk, di->num_sms);
+  if (n <= 1) return 0;
+  const size_t rows = (size_t)n * B * H * Nq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
+              float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  int st = check_shape(B, H, N, d, scale);
+  int st = check_shape(B, H, Nq, d, scale);
+  if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
   if (st != FA_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (workspace && !aligned16(workspace)))
+    return FA_ERR_MISALIGNED;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
   fa::FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   const int BH = B * H;
-  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128))
     return FA_ERR_LAUNCH;
+  a.o = o;
   a.lse = lse;
   a.status = di->status;
   a.BH = BH;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
   a.d = d;
   a.scale_log2 = (float)((double)scale * kLog2e);
   a.causal = causal ? 1 : 0;
+  // Key ranges: as many as help fill the GPU and fit the caller's workspace
+  // (none without one); every range non-empty.
+  const int nkv = (Nk + 127) / 128;
+  int n = workspace ? fa::pick_key_splits(BH, Nq, Nk, di->num_sms) : 1;
+  for (; n > 1; --n) {
+    const size_t rows = (size_t)n * BH * Nq;
+    if (align256(rows * d * sizeof(float)) + align256(rows * sizeof(float)) <= workspace_bytes) break;
+  }
+  a.split_blocks = (nkv + n - 1) / n;
+  a.n_split = (nkv + a.split_blocks - 1) / a.split_blocks;
+  if (a.n_split > 1) {
+    const size_t rows = (size_t)a.n_split * BH * Nq;
+    a.o_part = static_cast<float*>(workspace);
+    a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * d * sizeof(float)));
+  }
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -77,18 +77,33 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   volatile int* abort_flag = &bars.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
   int bh, blk;
   grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
   const int qblk = CAUSAL ? (int)gridDim.y - 1 - blk : blk;  // heaviest first under the causal mask
-  const int nkv = (N + C::BN - 1) / C::BN;
-  int nb[2];
+  const int nkv = (Nk + C::BN - 1) / C::BN;
+  // this CTA's key blocks: [jb, je) (all of them unless the keys are split)
+  const int jb = (int)blockIdx.z * a.split_blocks;
+  const int je = min(nkv, jb + a.split_blocks);
+  int nb[2];  // key blocks each query tile sees in the range, from jb on
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = qblk * 256 + t * 128;
-    nb[t] = r0 < N ? (CAUSAL ? min(r0 / C::BN + 1, nkv) : nkv) : 0;
+    const int last_key = CAUSAL ? min(min(r0 + 127, Nq - 1) + off, Nk - 1) : Nk - 1;
+    nb[t] = r0 < Nq ? max(0, min(last_key / C::BN + 1, je) - jb) : 0;
   }
   const int nb_max = max(nb[0], nb[1]);
+  if (nb_max == 0) {
+    // (key ranges only) no row of this CTA sees a key of its range: the range
+    // has no weight in the merge. The condition is uniform over the CTA, so
+    // every thread leaves before any barrier.
+    if (a.n_split > 1 && threadIdx.x < 256) {
+      const int row = qblk * 256 + (int)threadIdx.x;
+      if (row < Nq) a.lse_part[((size_t)blockIdx.z * a.BH + bh) * Nq + row] = -INFINITY;
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -149,7 +164,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[sk],
-                      pn * 64, j * C::BN, bh);
+                      pn * 64, (jb + j) * C::BN, bh);
       }
       __syncwarp();
       nk_issued = j + 1;
@@ -162,7 +177,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[sv],
-                      pn * 64, j * C::BN, bh);
+                      pn * 64, (jb + j) * C::BN, bh);
       }
       __syncwarp();
       nv_issued = j + 1;
@@ -269,7 +284,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // ------------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
-    const int row = qblk * 256 + t * 128 + r;
+    const int r0 = qblk * 256 + t * 128;
+    const int row = r0 + r;
     const int nbt = nb[t];
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::col_s(t);
@@ -290,10 +306,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-      const int kv0 = j * C::BN;
-      const bool need_mask = CAUSAL ? (j == nbt - 1) : (kv0 + C::BN > N);
+      // Only blocks that reach past the tile's first row's last key (the
+      // diagonal under the causal mask, one or two blocks) or past Nk need
+      // masking: there a hidden score becomes -inf, so P = 0 (scale > 0).
+      const int kv0 = (jb + j) * C::BN;
+      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > r0 + off) || kv0 + C::BN > Nk;
       if (need_mask) {
-        const int lim = CAUSAL ? (row - kv0) : (N - 1 - kv0);  // keep key column c iff c <= lim
+        const int lim = (CAUSAL ? min(row + off, Nk - 1) : Nk - 1) - kv0;  // keep key column c iff c <= lim
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -314,7 +333,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       const bool rescale = __any_sync(0xffffffffu, move && j > 0);
       float2 sum = make_float2(0.f, 0.f);
-      const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_ref, -m_ref);
+      // a row that has seen no key yet (possible within a key range) keeps m_ref = -inf and P = 0
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_use, -m_use);
       // P as bf16 pairs over the first 64 columns of S_t (all of S_t is already in
       // registers), 32 scores at a time.
 #pragma unroll
@@ -347,7 +368,29 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     }
     if (ok && nbt > 0) ok = mbar_wait(&bars.o_done[t], 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    if (nbt > 0) {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
+    if (a.n_split > 1) {
+      // O / l and the logsumexp of this key range, fp32, for the merge kernel
+      // (a row that saw no key of the range: lse = -inf, and the merge skips it)
+      const size_t prow = ((size_t)blockIdx.z * a.BH + bh) * Nq + row;
+      if (ok && nbt > 0) {
+        tc_fence_after();
+        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        float4* orow = reinterpret_cast<float4*>(a.o_part + prow * D);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_ld_wait(o);
+          if (row < Nq)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              orow[(c >> 2) + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                               __uint_as_float(o[4 * i + 2]) * inv_l,
+                                               __uint_as_float(o[4 * i + 3]) * inv_l);
+        }
+      }
+      if (ok && row < Nq) a.lse_part[prow] = nbt > 0 && l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    } else if (nbt > 0) {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
       uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is no longer read by any MMA
       if (ok) {
         tc_fence_after();
@@ -378,7 +421,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         bulk_commit();
         bulk_wait_read0();  // the staging tile has been read; the writes finish on their own
       }
-      if (ok && row < N) a.lse[(size_t)bh * N + row] = (m_ref + log2f(l_sum)) * kLn2;
+      if (ok && row < Nq) a.lse[(size_t)bh * Nq + row] = (m_ref + log2f(l_sum)) * kLn2;
     }
   }
 
@@ -388,14 +431,56 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   if (threadIdx.x == 0 && bars.abort) atomicOr(a.status, 1u);
 }
 
+// Merge of the key ranges' results, one warp per query row: with
+// m = max_z lse_z and w_z = e^(lse_z - m), o = sum_z w_z o_z / sum_z w_z and
+// lse = m + ln sum_z w_z (the running-maximum update of chapter 08 of
+// "FlashAttention and GPU Memory", for logsumexps, over all ranges at once).
+// A range the row sees no key of has lse_z = -inf and is skipped; every row
+// sees some key over all ranges, so m is finite.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const __grid_constant__ FwdArgs a) {
+  constexpr int V = D / 32;  // values of the row per lane
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)a.BH * a.Nq;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int z = 0; z < a.n_split; ++z) m = fmaxf(m, a.lse_part[z * rows + row]);
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  float tot = 0.f;
+  for (int z = 0; z < a.n_split; ++z) {
+    const float lz = a.lse_part[z * rows + row];
+    if (lz == -INFINITY) continue;
+    const float w = expf(lz - m);
+    tot += w;
+    const float* oz = a.o_part + (z * rows + row) * D + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] += w * oz[i];
+  }
+  const float inv = 1.f / tot;
+  uint32_t packed[V / 2];
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.o) + (row * D + lane * V) * 2);
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) dst[i] = packed[i];
+  if (lane == 0) a.lse[row] = m + logf(tot);
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fa_fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)a.BH, (unsigned)((a.N + 255) / 256));
+  const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + 255) / 256), (unsigned)a.n_split);
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  if (a.n_split > 1) {
+    const long long rows = (long long)a.BH * a.Nq;
+    fa_fwd_merge_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -404,7 +489,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdArgs& args, int num_sms, cudaStream_t stream) {
   FwdArgs a = args;
   // a CTA's fixed cost (loads before the first product, epilogue) is about two key blocks of work
-  a.head_group = pick_head_group(a.BH, (a.N + 255) / 256, a.causal != 0, num_sms, 2.0);
+  a.head_group = pick_head_group(a.BH, (a.Nq + 255) / 256, a.causal != 0, num_sms, 2.0);
   if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
   return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
 }

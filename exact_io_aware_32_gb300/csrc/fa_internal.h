@@ -9,13 +9,22 @@
 namespace fa {
 
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle
-  float* lse;                          // fp32 [BH][N]
-  unsigned int* status;                // device error word
-  int BH, N, d;
+  CUtensorMap tm_q, tm_o;  // bf16 [BH][Nq][d], box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_k, tm_v;  // bf16 [BH][Nk][d], the same boxes
+  void* o;                 // bf16 [BH][Nq][d] (written by the merge kernel when the keys are split)
+  float* lse;              // fp32 [BH][Nq]
+  unsigned int* status;    // device error word
+  int BH, Nq, Nk, d;
   float scale_log2;  // scale * log2(e)
-  int causal;
-  int head_group;  // heads per CTA scheduling group (set by launch_fwd)
+  int causal;        // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
+  int head_group;    // heads per CTA scheduling group (set by launch_fwd)
+  // Key ranges per query block. With n_split > 1, CTA z covers key blocks
+  // [z * split_blocks, (z + 1) * split_blocks) and writes O / l (fp32) and the
+  // range's logsumexp to o_part [n_split][BH][Nq][d] and lse_part
+  // [n_split][BH][Nq]; a merge kernel then writes o and lse.
+  int n_split, split_blocks;
+  float* o_part;
+  float* lse_part;
 };
 
 struct BwdArgs {
@@ -39,6 +48,11 @@ int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead)
 
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
+// Key ranges worth splitting a forward into (1 = no split): enough CTAs for
+// one per SM when the query blocks alone are fewer, each range at least two
+// 128-key blocks, at most kMaxKeySplits.
+constexpr int kMaxKeySplits = 32;
+int pick_key_splits(int BH, int Nq, int Nk, int num_sms);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace fa

@@ -92,4 +92,14 @@ int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead)
   return chosen;
 }
 
+int pick_key_splits(int BH, int Nq, int Nk, int num_sms) {
+  const long long ctas = (long long)BH * ((Nq + 255) / 256);  // CTAs without a split
+  const int nkv = (Nk + 127) / 128;
+  if (num_sms <= 0 || ctas >= num_sms || nkv < 4) return 1;
+  long long n = (num_sms + ctas - 1) / ctas;
+  n = std::min<long long>(n, nkv / 2);
+  n = std::min<long long>(n, kMaxKeySplits);
+  return (int)std::max<long long>(n, 1);
+}
+
 }  // namespace fa

@@ -1,11 +1,12 @@
 """Thin ctypes binding over libfa.so (include/fa.h).
 
 Argument marshalling only: every step of attention runs in the CUDA kernels
-of the library. The functions named like the C ABI (``fa_fwd``, ``fa_bwd``,
-``fa_bwd_workspace_bytes``, ``fa_status_string``, ``fa_device_status``,
-``fa_bwd_noalloc``) take
-either torch CUDA tensors or raw device addresses (ints). ``forward`` and
-``backward`` are conveniences that allocate the outputs with torch.
+of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
+``fa_fwd_kv_workspace_bytes``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
+``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
+torch CUDA tensors or raw device addresses (ints). ``forward``,
+``forward_kv`` and ``backward`` are conveniences that allocate the outputs
+with torch.
 
 If the library has not been built, or cannot be loaded, every call raises:
 there is no fallback implementation.
@@ -27,7 +28,8 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
+EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string",
+            "fa_device_status", "fa_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +61,11 @@ def load(path: str | None = None):
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, vp,
                                c_size_t, vp]
         lib.fa_bwd.restype = c_int
+        lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int, vp, c_size_t,
+                                  vp]
+        lib.fa_fwd_kv.restype = c_int
+        lib.fa_fwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
+        lib.fa_fwd_kv_workspace_bytes.restype = c_size_t
         lib.fa_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
         lib.fa_bwd_workspace_bytes.restype = c_size_t
         lib.fa_status_string.argtypes = [c_int]
@@ -100,6 +107,16 @@ def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal
                              int(bool(causal)), _stream(stream)))
 
 
+def fa_fwd_kv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_fwd_kv_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_fwd_kv(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: bool,
+              workspace=None, workspace_bytes: int = 0, stream=None) -> int:
+    return int(load().fa_fwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), B, H, Nq, Nk, d, float(scale),
+                                int(bool(causal)), _addr(workspace), int(workspace_bytes), _stream(stream)))
+
+
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_bytes(B, H, N, d))
 
@@ -132,6 +149,24 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     st = fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split: bool = True, stream=None):
+    """Nq query rows against Nk keys: allocate o, lse (and, with ``split``, the key-range
+    workspace fa_fwd_kv_workspace_bytes asks for) with torch and run fa_fwd_kv. Returns (o, lse)."""
+    import torch
+
+    B, H, Nq, d = _shape(q)
+    Nk = int(k.shape[2])
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = fa_fwd_kv_workspace_bytes(B, H, Nq, Nk, d) if split else 0
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
+    st = fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, ws, need, stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_kv")
     return o, lse
 
 

@@ -25,8 +25,11 @@
  * Conventions shared by every call:
  *   - q, k, v, o, dO, dq, dk, dv: bf16, contiguous [B, H, N, d], d innermost.
  *   - lse: fp32, contiguous [B, H, N].
- *   - Self-attention: queries and keys have the same length N.
- *   - causal != 0 masks key j for query i when j > i (row 0 sees key 0 only).
+ *   - Self-attention: queries and keys have the same length N, except in
+ *     fa_fwd_kv (Nq query rows against Nk keys).
+ *   - causal != 0 masks key j for query i when j > i (row 0 sees key 0 only);
+ *     with Nq != Nk the queries are the last Nq positions: key j is masked
+ *     for query i when j > i + Nk - Nq.
  *   - d must be 64 or 128. B, H, N >= 1, B * H * N * d < 2^31.
  *   - scale must be finite and > 0 (usually 1 / sqrt(d)).
  *   - Every pointer is a DEVICE pointer (the current CUDA device), 16-byte
@@ -72,6 +75,40 @@ typedef enum {
  */
 FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace with which fa_fwd_kv may split the keys of this
+ * shape over several CTAs per query block on the current device (0: the
+ * shape has enough query blocks to fill the GPU, or too few keys to split;
+ * also 0 for an invalid shape or without a usable device). The partial
+ * results are fp32 O / l [splits][B, H, Nq, d] and logsumexps
+ * [splits][B, H, Nq], each padded to 256 bytes.
+ */
+FA_API size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * Forward pass of Nq query rows against Nk keys, e.g. a decoding step (a few
+ * new queries against a long cache of keys and values) -- the unequal-length
+ * and decode-style attention the pages name as the next steps, computed as
+ * in fa_fwd with the query rows aligned to the last Nq keys under the mask.
+ *   q        [in]  bf16 [B, H, Nq, d]
+ *   k, v     [in]  bf16 [B, H, Nk, d]
+ *   o        [out] bf16 [B, H, Nq, d]
+ *   lse      [out] fp32 [B, H, Nq], lse[i] = ln sum_{j visible to i} exp(scale q_i . k_j)
+ *   causal   key j is visible to query i iff j <= i + Nk - Nq; needs Nq <= Nk
+ *            (FA_ERR_INVALID_ARG otherwise, since the first rows would see no key)
+ *   workspace, workspace_bytes
+ *            optional (NULL / 0: one pass over the keys per query block). With
+ *            fa_fwd_kv_workspace_bytes bytes (or fewer: then fewer ranges), a
+ *            call with few query blocks splits the keys into ranges, computes
+ *            each range's O / l and logsumexp, and merges them with the
+ *            running-maximum rule of chapter 08 written for logsumexps:
+ *            lse = m + ln sum_z e^(lse_z - m), o = sum_z e^(lse_z - lse) o_z.
+ * fa_fwd(..., N, ...) is fa_fwd_kv(..., N, N, ..., NULL, 0, stream).
+ * Returns FA_OK or an fa_status error code.
+ */
+FA_API int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                     int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: the fp32 row terms

@@ -73,6 +73,34 @@ def test_fwd_rejects_bad_args(lib, args, status):
 
 
 @pytest.mark.parametrize("args,status", [
+    (dict(v=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=1, Nq=65, Nk=64), fa.FA_ERR_INVALID_ARG),  # the first query row would see no key
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=1 << 28), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(ws=A + 8, ws_bytes=4096), fa.FA_ERR_MISALIGNED),
+])
+def test_fwd_kv_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Nq=8, Nk=64, d=128, scale=0.1, causal=0, ws=None, ws_bytes=0)
+    kw.update(args)
+    st = fa.fa_fwd_kv(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["B"], kw["H"], kw["Nq"], kw["Nk"], kw["d"],
+                      kw["scale"], kw["causal"], kw["ws"], kw["ws_bytes"], stream=0)
+    assert st == status
+
+
+def test_fwd_kv_workspace_bytes_without_gpu_or_bad_shape(lib):
+    import torch
+
+    assert fa.fa_fwd_kv_workspace_bytes(1, 1, 0, 16, 64) == 0
+    assert fa.fa_fwd_kv_workspace_bytes(1, 1, 4, 16, 96) == 0
+    if not torch.cuda.is_available():  # the split depends on the device's SM count
+        assert fa.fa_fwd_kv_workspace_bytes(1, 8, 1, 4096, 128) == 0
+
+
+@pytest.mark.parametrize("args,status", [
     (dict(dO=0), fa.FA_ERR_INVALID_ARG),
     (dict(d=32), fa.FA_ERR_UNSUPPORTED),
     (dict(dq=A + 2), fa.FA_ERR_MISALIGNED),
