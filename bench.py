@@ -13,6 +13,11 @@ divided by it. Rank 0 prints one JSON line.
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead
 (rank 0 only; other ranks exit at once), each step a bounded sample of the
 same workload.
+
+``--workload decode_<B>_<H>_<Nq>_<Nk>_<d>_<causal|noncausal>`` measures the
+decoding forward instead (fa_fwd_kv: Nq query rows against a resident cache of
+Nk keys and values, split over key ranges): a step is one call, and the metric
+is the HBM bandwidth of its algorithmic bytes.
 """
 from __future__ import annotations
 
@@ -34,6 +39,7 @@ if ROOT not in sys.path:
 from exact_io_aware_32_gb300 import inputs, model  # noqa: E402
 
 METRIC = "attention fwd and fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 peak"
+DECODE_METRIC = "decoding attention forward (fa_fwd_kv): GB/s of algorithmic HBM bytes (bf16, 1 GB300)"
 DEFAULT_WORKLOAD = "d128_n4096_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 L2_BYTES = 129e6
@@ -418,6 +424,129 @@ def run_gpu(args, w, causal: bool):
         print(json.dumps(result), flush=True)
 
 
+# ---------------------------------------------------------------------- decoding forward
+def decode_spec(name: str):
+    """'decode_<B>_<H>_<Nq>_<Nk>_<d>_<causal|noncausal>' -> dict, or None."""
+    if not name.startswith("decode_"):
+        return None
+    parts = name.split("_")
+    B, H, Nq, Nk, d = (int(x) for x in parts[1:6])
+    return dict(B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=parts[6] == "causal")
+
+
+def decode_bytes(c) -> int:
+    """Algorithmic bytes of one call: q, k, v read; o, lse written (the split's fp32 partials are overhead)."""
+    B, H, Nq, Nk, d = c["B"], c["H"], c["Nq"], c["Nk"], c["d"]
+    return B * H * (2 * Nq * d * 2 + 2 * Nk * d * 2 + Nq * 4)
+
+
+def run_decode(args, c):
+    import torch
+
+    from exact_io_aware_32_gb300 import fa
+    from oracle import oracle as orc
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+    scale = 1.0 / math.sqrt(d)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7000 + rank)
+    q = torch.randn((B, H, Nq, d), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, H, Nk, d), generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_fwd_kv_workspace_bytes(B, H, Nq, Nk, d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = int(stream.cuda_stream)
+
+    def call(xq=q, xo=o, xlse=lse):
+        st = fa.fa_fwd_kv(xq, k, v, xo, xlse, B, H, Nq, Nk, d, scale, causal, ws if ws_bytes else None, ws_bytes,
+                          sp)
+        if st:
+            raise fa.FAError(st, "fa_fwd_kv")
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.4)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    st = fa.fa_device_status(True)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "timed region")
+    t = sorted(e0.elapsed_time(e1) / 1e3 for e0, e1 in ev)
+    call_s = sum(t) / len(t)
+    nbytes = decode_bytes(c)
+    flops = 4.0 * B * H * Nq * Nk * d  # matmul flops, every key of every query counted
+    peaks = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # end to end: the cache stays on the device; every step copies its queries in and its results out
+    hq = q.to("cpu").pin_memory()
+    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        call()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = a0.elapsed_time(a1) / 1e3 / e2e_steps
+    # the oracle on a few heads of the same shape
+    cb = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = orc.max_threads(host_cores())
+        heads, secs = 0, 0.0
+        x = inputs.make_inputs(1, 1, Nq, d, seed=1)
+        y = inputs.make_inputs(1, 1, Nk, d, seed=2)
+        while heads < B * H and secs < args.cpu_budget:
+            t0 = time.perf_counter()
+            orc.fwd_kv(x["q"], y["k"], y["v"], scale, causal, nthreads=threads)
+            secs += time.perf_counter() - t0
+            heads += 1
+        cb = {"value": nbytes / (B * H) * heads / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+              "sample": f"{heads} of {B * H} heads, Nq={Nq}, Nk={Nk}, d={d}, fp64, {secs:.1f} s wall"}
+    if rank == 0:
+        splits = ws_bytes // max(1, (B * H * Nq * (d + 1) * 4)) if ws_bytes else 1
+        print(json.dumps({
+            "metric": DECODE_METRIC, "value": nbytes / call_s / 1e9, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": call_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, **c, "key_ranges_max": int(splits),
+                       "l2": f"k and v {2 * B * H * Nk * d * 2 / 1e6:.0f} MB per call vs 129 MB L2; no flush"},
+            "tflops": flops / call_s / 1e12,
+            "roofline": {"kernel": "fa_fwd_kv call: key-range forward + merge", "bound": "hbm",
+                         "achieved": nbytes / call_s / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": nbytes / call_s / 1e9 / hbm, "traffic": kernel_traffic("fa_fwd.cu", args.workload),
+                         "algorithmic_bytes_per_launch": nbytes},
+            "e2e": {"value": nbytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": hq.numel() * 2,
+                    "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "steps": e2e_steps,
+                    "schedule": "k, v resident (a cache); q in and o, lse out every step, one stream"},
+            "gpu_launches": args.steps * (2 if ws_bytes else 1), "clocks": clk, "cpu_baseline": cb,
+        }), flush=True)
+
+
 # ---------------------------------------------------------------------- reference arm (the oracle)
 def run_reference(args, w, causal: bool):
     rank, world, _ = dist_env()
@@ -468,6 +597,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    c = decode_spec(args.workload)
+    if c is not None:
+        if args.impl == "reference":
+            raise SystemExit("the decoding workloads have no reference arm")
+        run_decode(args, c)
+        return
     w, causal = workload_by_name(args.workload)
     if args.impl == "reference":
         run_reference(args, w, causal)

@@ -48,9 +48,9 @@ int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead)
 
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
-// Key ranges worth splitting a forward into (1 = no split): enough CTAs for
-// one per SM when the query blocks alone are fewer, each range at least two
-// 128-key blocks, at most kMaxKeySplits.
+// Key ranges worth splitting a forward into (1 = no split, when the query
+// blocks alone fill the SMs): the fewest whose CTAs fill their waves of one CTA
+// per SM to 90%, each range at least two 128-key blocks, at most kMaxKeySplits.
 constexpr int kMaxKeySplits = 32;
 int pick_key_splits(int BH, int Nq, int Nk, int num_sms);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);

@@ -96,10 +96,23 @@ int pick_key_splits(int BH, int Nq, int Nk, int num_sms) {
   const long long ctas = (long long)BH * ((Nq + 255) / 256);  // CTAs without a split
   const int nkv = (Nk + 127) / 128;
   if (num_sms <= 0 || ctas >= num_sms || nkv < 4) return 1;
-  long long n = (num_sms + ctas - 1) / ctas;
-  n = std::min<long long>(n, nkv / 2);
-  n = std::min<long long>(n, kMaxKeySplits);
-  return (int)std::max<long long>(n, 1);
+  // The fewest ranges whose CTAs fill their waves of one CTA per SM to 90%
+  // (a short last wave would double the time of a bandwidth-bound call), else
+  // the best filling; each range at least two key blocks.
+  const int cap = (int)std::min<long long>(kMaxKeySplits, nkv / 2);
+  int best = 1;
+  double best_fill = 0.0;
+  for (int n = 1; n <= cap; ++n) {
+    const long long total = ctas * n;
+    const long long waves = (total + num_sms - 1) / num_sms;
+    const double fill = (double)total / (double)(waves * num_sms);
+    if (fill >= 0.9) return n;
+    if (fill > best_fill) {
+      best_fill = fill;
+      best = n;
+    }
+  }
+  return best;
 }
 
 }  // namespace fa

@@ -92,3 +92,49 @@ def test_cached_answers_are_stable(picker):
     cases = [(128, 32, True, 152, 2.5)] * 3 + [(16, 128, True, 148, 2.5)] * 2
     out = picker(cases)
     assert len(set(out[:3])) == 1 and len(set(out[3:])) == 1
+
+
+SPLIT_DRIVER = r"""
+#include <cstdio>
+namespace fa { int pick_key_splits(int BH, int Nq, int Nk, int num_sms); }
+int main() {
+  int BH, Nq, Nk, sms;
+  while (scanf("%d %d %d %d", &BH, &Nq, &Nk, &sms) == 4) printf("%d\n", fa::pick_key_splits(BH, Nq, Nk, sms));
+  return 0;
+}
+"""
+
+
+@pytest.fixture(scope="module")
+def splitter(tmp_path_factory):
+    gxx = shutil.which("g++")
+    if not gxx:
+        pytest.skip("g++ not available")
+    d = tmp_path_factory.mktemp("split")
+    (d / "driver.cpp").write_text(SPLIT_DRIVER)
+    exe = d / "driver"
+    subprocess.check_call([gxx, "-O2", "-std=c++17", "-x", "c++", os.path.join(CSRC, "schedule.cu"), "-x", "c++",
+                           str(d / "driver.cpp"), "-I", CSRC, "-I", "/usr/local/cuda/include", "-o", str(exe)])
+
+    def pick(cases):
+        inp = "".join(f"{bh} {nq} {nk} {sms}\n" for bh, nq, nk, sms in cases)
+        return [int(x) for x in subprocess.run([str(exe)], input=inp, capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    return pick
+
+
+def test_key_splits(splitter):
+    """No split once the query blocks fill the SMs or the keys are few; otherwise the fewest ranges
+    whose CTAs fill their waves (one CTA per SM) to 90%, each range >= 2 key blocks, at most 32."""
+    cases = [(256, 1, 16384, 152), (128, 4096, 4096, 152), (8, 1, 256, 152), (32, 128, 32768, 152),
+             (32, 1, 65536, 152), (1, 1, 1 << 20, 152), (2, 4096, 4096, 152), (3, 1, 1000, 152)]
+    got = splitter(cases)
+    assert got[0] == 1 and got[1] == 1 and got[2] == 1
+    for (bh, nq, nk, sms), n in zip(cases[3:], got[3:]):
+        ctas = bh * ((nq + 255) // 256)
+        nkv = (nk + 127) // 128
+        assert 1 <= n <= min(32, nkv // 2)
+        fill = lambda m: ctas * m / (-(-ctas * m // sms) * sms)  # noqa: E731
+        better = [m for m in range(1, min(32, nkv // 2) + 1) if fill(m) >= 0.9]
+        assert n == (better[0] if better else max(range(1, min(32, nkv // 2) + 1), key=lambda m: (fill(m), -m)))
+    assert got[3] == 9  # 32 heads x 1 query block: 288 CTAs = 95% of two waves
