@@ -56,8 +56,6 @@ static double dot(const double* a, const double* b, int d) {
   return acc;
 }
 
-static int row_len(int i, int N, int causal) { return causal ? i + 1 : N; }
-
 /* Keys visible to query row i of Nq against Nk keys. */
 static int row_len_kv(int i, int Nq, int Nk, int causal) { return causal ? i + 1 + (Nk - Nq) : Nk; }
 
@@ -138,40 +136,43 @@ int oracle_fwd(const double* q, const double* k, const double* v, double* o, dou
 }
 
 /*
- * Backward pass. Every row's lse and D are computed (both are needed by every
- * key's gradient). dq is written for the listed query rows (qrows == NULL:
- * all rows), dk and dv for the listed keys (keys == NULL: all keys). D, if
- * non-NULL, receives D_i for every row. Returns 0, or -1 on error.
+ * Backward pass, Nq query rows against Nk keys (causal: row i sees keys
+ * 0..i + Nk - Nq; needs Nq <= Nk). Every row's lse and D are computed (both
+ * are needed by every key's gradient). dq is written for the listed query rows
+ * (qrows == NULL: all rows), dk and dv for the listed keys (keys == NULL: all
+ * keys). D, if non-NULL, receives D_i for every row. Returns 0, or -1 on error.
  */
-int oracle_bwd(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
-               double* dv, double* D, int BH, int N, int d, double scale, int causal, const int* qrows, int nq,
-               const int* keys, int nk, int nthreads) {
-  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !dO || !dq || !dk || !dv) return -1;
-  if (!qrows) nq = N;
-  if (!keys) nk = N;
-  for (int r = 0; qrows && r < nq; ++r)
-    if (qrows[r] < 0 || qrows[r] >= N) return -1;
-  for (int r = 0; keys && r < nk; ++r)
-    if (keys[r] < 0 || keys[r] >= N) return -1;
+int oracle_bwd_kv(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
+                  double* dv, double* D, int BH, int Nq, int Nk, int d, double scale, int causal, const int* qrows,
+                  int nqr, const int* keys, int nkr, int nthreads) {
+  if (BH < 1 || Nq < 1 || Nk < 1 || d < 1 || !q || !k || !v || !dO || !dq || !dk || !dv) return -1;
+  if (causal && Nq > Nk) return -1;
+  const int off = Nk - Nq;
+  if (!qrows) nqr = Nq;
+  if (!keys) nkr = Nk;
+  for (int r = 0; qrows && r < nqr; ++r)
+    if (qrows[r] < 0 || qrows[r] >= Nq) return -1;
+  for (int r = 0; keys && r < nkr; ++r)
+    if (keys[r] < 0 || keys[r] >= Nk) return -1;
   set_threads(nthreads);
-  double* lse_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
-  double* D_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
-  char* want_q = (char*)calloc((size_t)N, 1);
+  double* lse_all = (double*)malloc(sizeof(double) * (size_t)BH * Nq);
+  double* D_all = (double*)malloc(sizeof(double) * (size_t)BH * Nq);
+  char* want_q = (char*)calloc((size_t)Nq, 1);
   if (!lse_all || !D_all || !want_q) {
     free(lse_all);
     free(D_all);
     free(want_q);
     return -1;
   }
-  for (int r = 0; r < nq; ++r) want_q[qrows ? qrows[r] : r] = 1;
+  for (int r = 0; r < nqr; ++r) want_q[qrows ? qrows[r] : r] = 1;
   int failed = 0;
 
   /* Pass 1, one query row at a time: P, dP, D and dS of the row; dq. */
-  const long long total_rows = (long long)BH * N;
+  const long long total_rows = (long long)BH * Nq;
 #pragma omp parallel
   {
-    double* s = (double*)malloc(sizeof(double) * (size_t)N);
-    double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)Nk);
     if (!s || !dp) {
 #pragma omp atomic write
       failed = 1;
@@ -179,27 +180,27 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 #pragma omp for schedule(dynamic, 4)
     for (long long w = 0; w < total_rows; ++w) {
       if (!s || !dp) continue;
-      const int h = (int)(w / N), i = (int)(w % N);
-      const size_t hb = (size_t)h * N * d;
-      const double* qi = q + hb + (size_t)i * d;
-      const double* dOi = dO + hb + (size_t)i * d;
-      const int n = row_len(i, N, causal);
+      const int h = (int)(w / Nq), i = (int)(w % Nq);
+      const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nk * d;
+      const double* qi = q + qb + (size_t)i * d;
+      const double* dOi = dO + qb + (size_t)i * d;
+      const int n = row_len_kv(i, Nq, Nk, causal);
       double M, l;
-      score_row(qi, k + hb, n, d, scale, s, &M, &l);
+      score_row(qi, k + kb, n, d, scale, s, &M, &l);
       double Di = 0.0;
       for (int j = 0; j < n; ++j) {
         s[j] = exp(s[j] - M) / l; /* s now holds P_ij */
-        dp[j] = dot(dOi, v + hb + (size_t)j * d, d);
+        dp[j] = dot(dOi, v + kb + (size_t)j * d, d);
         Di += s[j] * dp[j];
       }
       lse_all[w] = M + log(l);
       D_all[w] = Di;
       if (want_q[i]) {
-        double* dqi = dq + hb + (size_t)i * d;
+        double* dqi = dq + qb + (size_t)i * d;
         for (int t = 0; t < d; ++t) dqi[t] = 0.0;
         for (int j = 0; j < n; ++j) {
           const double ds = s[j] * (dp[j] - Di);
-          const double* kj = k + hb + (size_t)j * d;
+          const double* kj = k + kb + (size_t)j * d;
           for (int t = 0; t < d; ++t) dqi[t] += scale * ds * kj[t];
         }
       }
@@ -209,26 +210,26 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
   }
 
   /* Pass 2, one key at a time: dk and dv sum over the rows that see key j. */
-  const long long total_keys = (long long)BH * nk;
+  const long long total_keys = (long long)BH * nkr;
   if (!failed) {
 #pragma omp parallel for schedule(dynamic, 4)
     for (long long w = 0; w < total_keys; ++w) {
-      const int h = (int)(w / nk);
-      const int j = keys ? keys[w % nk] : (int)(w % nk);
-      const size_t hb = (size_t)h * N * d;
-      const double* kj = k + hb + (size_t)j * d;
-      const double* vj = v + hb + (size_t)j * d;
-      double* dkj = dk + hb + (size_t)j * d;
-      double* dvj = dv + hb + (size_t)j * d;
+      const int h = (int)(w / nkr);
+      const int j = keys ? keys[w % nkr] : (int)(w % nkr);
+      const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nk * d;
+      const double* kj = k + kb + (size_t)j * d;
+      const double* vj = v + kb + (size_t)j * d;
+      double* dkj = dk + kb + (size_t)j * d;
+      double* dvj = dv + kb + (size_t)j * d;
       for (int t = 0; t < d; ++t) {
         dkj[t] = 0.0;
         dvj[t] = 0.0;
       }
-      for (int i = causal ? j : 0; i < N; ++i) {
-        const double* qi = q + hb + (size_t)i * d;
-        const double* dOi = dO + hb + (size_t)i * d;
-        const double p = exp(scale * dot(qi, kj, d) - lse_all[(size_t)h * N + i]);
-        const double ds = p * (dot(dOi, vj, d) - D_all[(size_t)h * N + i]);
+      for (int i = causal && j > off ? j - off : 0; i < Nq; ++i) {
+        const double* qi = q + qb + (size_t)i * d;
+        const double* dOi = dO + qb + (size_t)i * d;
+        const double p = exp(scale * dot(qi, kj, d) - lse_all[(size_t)h * Nq + i]);
+        const double ds = p * (dot(dOi, vj, d) - D_all[(size_t)h * Nq + i]);
         for (int t = 0; t < d; ++t) {
           dkj[t] += scale * ds * qi[t];
           dvj[t] += p * dOi[t];
@@ -236,11 +237,18 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
       }
     }
   }
-  if (D && !failed) memcpy(D, D_all, sizeof(double) * (size_t)BH * N);
+  if (D && !failed) memcpy(D, D_all, sizeof(double) * (size_t)BH * Nq);
   free(lse_all);
   free(D_all);
   free(want_q);
   return failed ? -1 : 0;
+}
+
+/* Backward pass of self-attention (Nq = Nk = N). */
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
+               double* dv, double* D, int BH, int N, int d, double scale, int causal, const int* qrows, int nq,
+               const int* keys, int nk, int nthreads) {
+  return oracle_bwd_kv(q, k, v, dO, dq, dk, dv, D, BH, N, N, d, scale, causal, qrows, nq, keys, nk, nthreads);
 }
 
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */

@@ -72,6 +72,9 @@ def load(path: str | None = None):
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int,
                                    ip, c_int, ip, c_int, c_int]
         lib.oracle_bwd.restype = c_int
+        lib.oracle_bwd_kv.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int,
+                                      ip, c_int, ip, c_int, c_int]
+        lib.oracle_bwd_kv.restype = c_int
         lib.oracle_max_threads.argtypes = [c_int]
         lib.oracle_max_threads.restype = c_int
         if path is None:
@@ -169,6 +172,29 @@ def bwd(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads
                         None if ki is None else ki.ctypes.data_as(ip), nk, nthreads)
     if rc != 0:
         raise RuntimeError("oracle_bwd failed")
+    return dq, dk, dv, D
+
+
+def bwd_kv(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads: int = 0, lib=None):
+    """dq [BH, Nq, d], dk and dv [BH, Nk, d] and D [BH, Nq] for Nq query rows against Nk keys, fp64
+    (causal: row i sees keys <= i + Nk - Nq; needs Nq <= Nk). ``qrows`` / ``keys`` as in ``bwd``."""
+    lib = lib or load()
+    q3, k3, v3, dO3 = (_as3(_f64(x)) for x in (q, k, v, dO))
+    BH, Nq, d = q3.shape
+    Nk = k3.shape[1]
+    dq = np.full_like(q3, np.nan)
+    dk = np.full_like(k3, np.nan)
+    dv = np.full_like(k3, np.nan)
+    D = np.full((BH, Nq), np.nan)
+    qi, nq = _iptr(qrows)
+    ki, nk = _iptr(keys)
+    ip = ctypes.POINTER(ctypes.c_int)
+    rc = lib.oracle_bwd_kv(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(dO3), _dptr(dq), _dptr(dk), _dptr(dv), _dptr(D),
+                           BH, Nq, Nk, d, float(scale), int(causal),
+                           None if qi is None else qi.ctypes.data_as(ip), nq,
+                           None if ki is None else ki.ctypes.data_as(ip), nk, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_bwd_kv failed (causal needs Nq <= Nk)")
     return dq, dk, dv, D
 
 

@@ -293,6 +293,44 @@ def pin_kv_merge_of_key_ranges(lib=None):
     assert np.allclose(om2, o, rtol=0, atol=1e-14) and np.allclose(lm2, lse, rtol=0, atol=1e-13)
 
 
+def pin_kv_bwd_torch_autograd(lib=None):
+    """dq, dk, dv for Nq != Nk against torch fp64 SDPA + autograd with the explicit bottom-right mask."""
+    for seed, (BH, Nq, Nk, d) in enumerate([(2, 3, 11, 8), (1, 9, 9, 4), (2, 12, 5, 8)]):
+        q, k, v = _kv(140 + seed, BH, Nq, Nk, d)
+        dO = np.random.default_rng(150 + seed).standard_normal((BH, Nq, d))
+        for causal in (False, True):
+            if causal and Nq > Nk:
+                continue
+            mask = torch.tensor(np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)) if causal else None
+            tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+            o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.55)
+            o.backward(torch.tensor(dO))
+            dq, dk, dv, D = orc.bwd_kv(q, k, v, dO, 0.55, causal, lib=lib)
+            for g, r in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+                assert np.allclose(g, r.numpy(), rtol=0, atol=1e-12), (Nq, Nk, causal)
+            assert np.allclose(D, np.einsum("bid,bid->bi", dO, o.detach().numpy()), rtol=0, atol=1e-12)
+
+
+def pin_kv_bwd_suffix_of_self_attention(lib=None):
+    """Causal, Nq < Nk: the gradients equal those of self-attention over Nk rows whose first
+    Nk - Nq rows have any queries and a zero output gradient (such rows add nothing to dk, dv)."""
+    BH, Nq, Nk, d = 2, 5, 14, 8
+    q, k, v = _kv(160, BH, Nq, Nk, d)
+    dO = np.random.default_rng(161).standard_normal((BH, Nq, d))
+    head = np.random.default_rng(162).standard_normal((BH, Nk - Nq, d))
+    dq_f, dk_f, dv_f, _ = orc.bwd(np.concatenate([head, q], axis=1), k, v,
+                                  np.concatenate([np.zeros_like(head), dO], axis=1), 0.6, True, lib=lib)
+    dq, dk, dv, _ = orc.bwd_kv(q, k, v, dO, 0.6, True, lib=lib)
+    assert np.allclose(dq, dq_f[:, Nk - Nq:], rtol=0, atol=1e-13)
+    assert np.allclose(dk, dk_f, rtol=0, atol=1e-13) and np.allclose(dv, dv_f, rtol=0, atol=1e-13)
+    q, k, v = _kv(163, 1, 7, 7, 4)
+    dO = np.random.default_rng(164).standard_normal((1, 7, 4))
+    for causal in (False, True):
+        a = orc.bwd_kv(q, k, v, dO, 0.6, causal, lib=lib)
+        b = orc.bwd(q, k, v, dO, 0.6, causal, lib=lib)
+        assert all(np.allclose(x, y, rtol=0, atol=1e-15) for x, y in zip(a, b))
+
+
 ALL_PINS = [
     pin_zero_q_noncausal,
     pin_zero_q_causal,
@@ -311,4 +349,6 @@ ALL_PINS = [
     pin_kv_suffix_of_self_attention,
     pin_kv_single_key_and_last_row,
     pin_kv_merge_of_key_ranges,
+    pin_kv_bwd_torch_autograd,
+    pin_kv_bwd_suffix_of_self_attention,
 ]

@@ -14,18 +14,23 @@ SRC = os.path.join(os.path.dirname(orc.__file__), "fa_oracle.c")
 # (name, text in the oracle source, replacement)
 MUTANTS = [
     ("dropped_scale", "s[j] = scale * dot(qi, k + (size_t)j * d, d);", "s[j] = dot(qi, k + (size_t)j * d, d);"),
-    ("causal_excludes_diagonal", "return causal ? i + 1 : N;", "return causal ? (i > 0 ? i : 1) : N;"),
+    ("causal_excludes_diagonal", "return causal ? i + 1 + (Nk - Nq) : Nk;",
+     "return causal ? (i > 0 ? i + (Nk - Nq) : 1 + (Nk - Nq)) : Nk;"),
     ("lse_without_log_sum", "lse[(size_t)h * Nq + i] = M + log(l);", "lse[(size_t)h * Nq + i] = M;"),
     ("output_reads_k_not_v", "const double* vh = v + (size_t)h * Nk * d;", "const double* vh = k + (size_t)h * Nk * d;"),
     ("kv_causal_top_left", "return causal ? i + 1 + (Nk - Nq) : Nk;", "return causal ? i + 1 : Nk;"),
     ("kv_query_head_stride", "const double* qi = q + ((size_t)h * Nq + i) * d;", "const double* qi = q + ((size_t)h * Nk + i) * d;"),
+    ("bwd_kv_key_head_stride", "const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nk * d;\n      const double* kj",
+     "const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nq * d;\n      const double* kj"),
     ("D_wrong_sign", "Di += s[j] * dp[j];", "Di -= s[j] * dp[j];"),
     ("dq_dropped_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
     ("dk_transposed_operand", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
     ("dv_uses_dS", "dvj[t] += p * dOi[t];", "dvj[t] += ds * dOi[t];"),
-    ("bwd_causal_skips_diagonal", "for (int i = causal ? j : 0; i < N; ++i)", "for (int i = causal ? j + 1 : 0; i < N; ++i)"),
-    ("bwd_mask_reversed", "for (int i = causal ? j : 0; i < N; ++i)", "for (int i = 0; i < (causal ? j + 1 : N); ++i)"),
-    ("dp_uses_o_index", "dp[j] = dot(dOi, v + hb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + hb + (size_t)i * d, d);"),
+    ("bwd_causal_skips_diagonal", "for (int i = causal && j > off ? j - off : 0; i < Nq; ++i)",
+     "for (int i = causal && j >= off ? j - off + 1 : 0; i < Nq; ++i)"),
+    ("bwd_mask_reversed", "for (int i = causal && j > off ? j - off : 0; i < Nq; ++i)",
+     "for (int i = 0; i < (causal ? (j - off + 1 > 0 ? j - off + 1 : 0) : Nq) && i < Nq; ++i)"),
+    ("dp_uses_o_index", "dp[j] = dot(dOi, v + kb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + kb + (size_t)i * d, d);"),
 ]
 
 
