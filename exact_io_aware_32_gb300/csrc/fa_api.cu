@@ -161,22 +161,32 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) { return fa_bwd_kv_workspace_bytes(B, H, N, N, d); }
+
+size_t fa_bwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (check_shape(B, H, Nq, d, 1.0f) != FA_OK || check_shape(B, H, Nk, d, 1.0f) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * Nq;
   return align256(rows * sizeof(float)) + 256;  // D, then the kernels' work counters
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
            size_t workspace_bytes, void* stream) {
+  return fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+              void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  int st = check_shape(B, H, N, d, scale);
+  int st = check_shape(B, H, Nq, d, scale);
+  if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
   if (st != FA_OK) return st;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_MISALIGNED;
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  const size_t need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return FA_ERR_WORKSPACE;
   DeviceInfo* di = nullptr;
@@ -186,20 +196,21 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   std::memset(&a, 0, sizeof(a));
   a.Dsum = static_cast<float*>(workspace);
   a.work = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + (need - 256));
-  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
-      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128))
     return FA_ERR_LAUNCH;
   a.o = o;
   a.dO = dO;
   a.lse = lse;
   a.status = di->status;
   a.BH = BH;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
   a.d = d;
   a.scale = scale;
   a.scale_log2 = (float)((double)scale * kLog2e);

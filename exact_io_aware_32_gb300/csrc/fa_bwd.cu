@@ -154,10 +154,13 @@ struct DkdvTile {
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nq) {
+__device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nq, int nkv) {
   DkdvTile t;
-  grouped_index(L, a.BH, nq, a.head_group, t.bh, t.kblk);  // key block 0 (the heaviest) first
-  t.i_start = CAUSAL ? t.kblk : 0;                          // BQ == BK: query block i sees key block j iff i >= j
+  grouped_index(L, a.BH, nkv, a.head_group, t.bh, t.kblk);  // key block 0 (the heaviest) first
+  // BQ == BK: query block i sees key block j iff its last row does, 128 i + 127 + Nk - Nq >= 128 j
+  // (with Nq = Nk: iff i >= j). The last query row sees every key, so n >= 1.
+  const int x = t.kblk * 128 - 127 - (a.Nk - a.Nq);
+  t.i_start = CAUSAL && x > 0 ? (x + 127) / 128 : 0;
   t.n = nq - t.i_start;
   return t;
 }
@@ -176,9 +179,11 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
   float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N;
-  const int nq = (N + C::BQ - 1) / C::BQ;
-  const int total = a.BH * nq;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
+  const int nq = (Nq + C::BQ - 1) / C::BQ;
+  const int nkv = (Nk + C::BK - 1) / C::BK;
+  const int total = a.BH * nkv;
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
       if (L >= total) break;
-      const DkdvTile t = dkdv_tile<CAUSAL>(L, a, nq);
+      const DkdvTile t = dkdv_tile<CAUSAL>(L, a, nq, nkv);
       bars.st_bh[k & 7] = t.bh;  // every lane writes the same values
       bars.st_kblk[k & 7] = t.kblk;
       bars.st_last[k & 7] = g + t.n - 1;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
           tiles_done = true;
           return Blk{0, 0, -1};
         }
-        cursor = Blk{0, dkdv_tile<CAUSAL>(L, a, nq).n, cursor.kt + 1};
+        cursor = Blk{0, dkdv_tile<CAUSAL>(L, a, nq, nkv).n, cursor.kt + 1};
         return cursor;
       };
       if (warp == 10) {
@@ -540,21 +545,21 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
     // later, so that no thread waits for the load in between.
     auto fetch = [&](const DkdvTile& t, int qb) -> float {
       const int q = qb * C::BQ + 64 * w + (tt & 63);
-      if (tt < 64) return q < N ? a.lse[(size_t)t.bh * N + q] : INFINITY;  // 2^(x - inf) = 0 past N
-      return q < N ? a.Dsum[(size_t)t.bh * N + q] : 0.f;
+      if (tt < 64) return q < Nq ? a.lse[(size_t)t.bh * Nq + q] : INFINITY;  // 2^(x - inf) = 0 past Nq
+      return q < Nq ? a.Dsum[(size_t)t.bh * Nq + q] : 0.f;
     };
     // After a failed wait a warp keeps going without work; at every block the
     // group's named barrier also ANDs the warps' states, so the four warps
     // always agree on their blocks and tiles and meet at the same barriers.
     int L = take_tile(0);
-    DkdvTile t = L >= 0 ? dkdv_tile<CAUSAL>(L, a, nq) : DkdvTile{0, 0, 0, 0};
+    DkdvTile t = L >= 0 ? dkdv_tile<CAUSAL>(L, a, nq, nkv) : DkdvTile{0, 0, 0, 0};
     float next = L >= 0 ? fetch(t, t.i_start) : 0.f;
     bool ok = L >= 0;
     int g = 0;
     for (int k = 0; L >= 0; ++k) {
       const int key = t.kblk * C::BK + r;
-      const bool key_ok = key < N;
-      const bool keys_all_ok = (t.kblk + 1) * C::BK <= N;  // uniform over the CTA
+      const bool key_ok = key < Nk;
+      const bool keys_all_ok = (t.kblk + 1) * C::BK <= Nk;  // uniform over the CTA
       int L_next = -1;
       DkdvTile nt = {0, 0, 0, 0};
       for (int it = 0; it < t.n; ++it, ++g) {
@@ -567,7 +572,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
         } else {  // the next tile's first block
           L_next = take_tile(k + 1);
           if (L_next >= 0) {
-            nt = dkdv_tile<CAUSAL>(L_next, a, nq);
+            nt = dkdv_tile<CAUSAL>(L_next, a, nq, nkv);
             next = fetch(nt, nt.i_start);
           }
         }
@@ -588,11 +593,13 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
           tmem_ld_wait(sr[1]);
           tc_fence_before();
           mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
-          // Only the diagonal block (the first under the causal mask) and a ragged
-          // last key block need masking: there a hidden score becomes -inf, so P = 0
-          // (scale > 0). Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col >= key.
-          if ((CAUSAL && it == 0) || !keys_all_ok) {
-            const int lim = CAUSAL && it == 0 ? key - (q0 + 64 * w) : -1;  // drop columns col < lim
+          // Only blocks whose first query row does not see the block's last key
+          // (the diagonal, the first block under the causal mask; a second one when
+          // Nk - Nq is not a multiple of 128) and a ragged last key block need
+          // masking: there a hidden score becomes -inf, so P = 0 (scale > 0).
+          // Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col + off >= key.
+          if ((CAUSAL && q0 + off < (t.kblk + 1) * C::BK - 1) || !keys_all_ok) {
+            const int lim = CAUSAL ? key - off - (q0 + 64 * w) : -1;  // drop columns col < lim
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c < lim || !key_ok) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -750,12 +757,13 @@ struct DqTile {
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq) {
+__device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq, int nkv) {
   DqTile t;
   int blk;
-  grouped_index(L, a.BH, nq, a.head_group, t.bh, blk);
+  grouped_index(L, a.BH, nq, a.head_group_dq, t.bh, blk);
   t.qblk = CAUSAL ? nq - 1 - blk : blk;  // heaviest first under the causal mask
-  t.nk = CAUSAL ? t.qblk + 1 : nq;       // BQ == BK: query block i sees key blocks 0..i
+  // BQ == BK: query block i sees key blocks 0 .. (128 i + 127 + Nk - Nq) / 128 (with Nq = Nk: 0..i)
+  t.nk = CAUSAL ? min((t.qblk * 128 + 127 + a.Nk - a.Nq) / 128 + 1, nkv) : nkv;
   return t;
 }
 
@@ -768,8 +776,10 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
   volatile int* abort_flag = &bars.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N;
-  const int nq = (N + C::BQ - 1) / C::BQ;
+  const int Nq = a.Nq, Nk = a.Nk;
+  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
+  const int nq = (Nq + C::BQ - 1) / C::BQ;
+  const int nkv = (Nk + C::BK - 1) / C::BK;
   const int total = a.BH * nq;
 
   if (threadIdx.x == 0) {
@@ -875,7 +885,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
       if (L >= total) break;
-      const DqTile t = dq_tile<CAUSAL>(L, a, nq);
+      const DqTile t = dq_tile<CAUSAL>(L, a, nq, nkv);
       if (k == 1 && !(ok = warp_wait(&bars.qt_ready, 0, abort_flag))) break;
       if (k >= 2 && !(ok = store_dq(k - 2, false))) break;
       if (k & 1)
@@ -956,7 +966,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
         int k = 0, g = 0;  // tile and key block over the CTA's run
         bool ok = true;
         for (int L = take_tile(0); ok && L >= 0; L = take_tile(++k)) {
-          const DqTile t = dq_tile<CAUSAL>(L, a, nq);
+          const DqTile t = dq_tile<CAUSAL>(L, a, nq, nkv);
           for (int j = 0; j < t.nk; ++j) {
             const int gj = g + j;
             if (!(ok = warp_wait2(&bars.ds_ready, gj & 1, &bars.k_full[gj % C::kKStages], k_phase(gj), abort_flag)))
@@ -1009,7 +1019,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
         };
         int k = 0, g = 0;  // tile and key block over the CTA's run
         int L = take_tile(0);
-        DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
+        DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq, nkv) : DqTile{0, 0, 0};
         bool ok = L >= 0;
         while (ok) {
           // the tile's first block: S needs its Q in TMEM (the warpgroups copy it
@@ -1040,7 +1050,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
           g += t.nk;
           ++k;
           if ((L = take_tile(k)) < 0) break;
-          t = dq_tile<CAUSAL>(L, a, nq);
+          t = dq_tile<CAUSAL>(L, a, nq, nkv);
         }
         if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
         __syncwarp();
@@ -1057,14 +1067,14 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;
     const uint32_t t_ds = tmem + lane_off + C::kColDS + 32 * w;
     // this thread's row terms for a tile, loaded early and converted when
-    // the tile starts (rows past N read row N-1 and get P = 0 then)
+    // the tile starts (rows past Nq read row Nq - 1 and get P = 0 then)
     auto load_row_terms = [&](const DqTile& t, float& lse_raw, float& d_raw) {
-      const int q = min(t.qblk * C::BQ + r, N - 1);
-      lse_raw = a.lse[(size_t)t.bh * N + q];
-      d_raw = a.Dsum[(size_t)t.bh * N + q];
+      const int q = min(t.qblk * C::BQ + r, Nq - 1);
+      lse_raw = a.lse[(size_t)t.bh * Nq + q];
+      d_raw = a.Dsum[(size_t)t.bh * Nq + q];
     };
     auto row_terms = [&](const DqTile& t, float lse_raw, float d_raw, float& lse2, float& dsum) {
-      const bool in = t.qblk * C::BQ + r < N;
+      const bool in = t.qblk * C::BQ + r < Nq;
       lse2 = in ? lse_raw * kLog2e : INFINITY;
       dsum = in ? d_raw : 0.f;
     };
@@ -1085,7 +1095,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     int k = 0, g = 0;
     int L = take_tile(0);
     bool ok = L >= 0;
-    DqTile t = ok ? dq_tile<CAUSAL>(L, a, nq) : DqTile{0, 0, 0};
+    DqTile t = ok ? dq_tile<CAUSAL>(L, a, nq, nkv) : DqTile{0, 0, 0};
     float lse2 = 0.f, dsum = 0.f;
     if (ok) {
       float lr, dr;
@@ -1113,10 +1123,12 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
           tmem_ld_wait(sr[1]);
           tc_fence_before();
           mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
-          // Only the diagonal block and a ragged last key block need masking: keys
-          // past the causal diagonal or past N get a -inf score, so P = 0 (scale > 0).
-          if ((CAUSAL && j == t.qblk) || (j + 1) * C::BK > N) {
-            const int lim = (CAUSAL ? min(q, N - 1) : N - 1) - k0;  // keep key k0 + col iff col <= lim
+          // Only blocks reaching past the tile's first row's last key (the diagonal,
+          // or two blocks when Nk - Nq is not a multiple of 128) and a ragged last
+          // key block need masking: keys past the causal limit or past Nk get a
+          // -inf score, so P = 0 (scale > 0).
+          if ((CAUSAL && (j + 1) * C::BK - 1 > t.qblk * C::BQ + off) || (j + 1) * C::BK > Nk) {
+            const int lim = (CAUSAL ? min(q + off, Nk - 1) : Nk - 1) - k0;  // keep key k0 + col iff col <= lim
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -1184,7 +1196,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
       DqTile nt = {0, 0, 0};
       float lse_next = 0.f, d_next = 0.f;
       if (L >= 0) {
-        nt = dq_tile<CAUSAL>(L, a, nq);
+        nt = dq_tile<CAUSAL>(L, a, nq, nkv);
         load_row_terms(nt, lse_next, d_next);
         ok = copy_q(k + 1);
       }
@@ -1223,7 +1235,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int kThreadsPerRow = D / 8;
-  const long long rows = (long long)a.BH * a.N;
+  const long long rows = (long long)a.BH * a.Nq;
   const long long row = (long long)blockIdx.x * (256 / kThreadsPerRow) + threadIdx.x / kThreadsPerRow;
   const int part = threadIdx.x % kThreadsPerRow;
   float acc = 0.f;
@@ -1245,25 +1257,24 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant_
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
-  const long long rows = (long long)a.BH * a.N;
+  const long long rows = (long long)a.BH * a.Nq;
   const int rows_per_block = 256 / (D / 8);
   fa_bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned nblk = (unsigned)((a.N + 127) / 128);
   auto kv = fa_bwd_dkdv_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
   // persistent: one CTA per SM at most (both main kernels take their tiles from counters)
-  const long long tiles = (long long)a.BH * nblk;
-  kv<<<(unsigned)std::min<long long>(tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
+  const long long kv_tiles = (long long)a.BH * ((a.Nk + 127) / 128), q_tiles = (long long)a.BH * ((a.Nq + 127) / 128);
+  kv<<<(unsigned)std::min<long long>(kv_tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kq = fa_bwd_dq_kernel<D, CAUSAL>;
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
-  kq<<<(unsigned)std::min<long long>(tiles, num_sms), 352, DqCfg<D>::kSmemBytes, stream>>>(a);
+  kq<<<(unsigned)std::min<long long>(q_tiles, num_sms), 352, DqCfg<D>::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -1272,7 +1283,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
 cudaError_t launch_bwd(const BwdArgs& args, int num_sms, cudaStream_t stream) {
   BwdArgs a = args;
   // a CTA's fixed cost (loads before the first product, epilogue) is about 2.5 blocks of work
-  a.head_group = pick_head_group(a.BH, (a.N + 127) / 128, a.causal != 0, num_sms, 2.5);
+  a.head_group = pick_head_group(a.BH, (a.Nk + 127) / 128, a.causal != 0, num_sms, 2.5);
+  a.head_group_dq = pick_head_group(a.BH, (a.Nq + 127) / 128, a.causal != 0, num_sms, 2.5);
   if (a.d == 64)
     return a.causal ? launch_bwd_t<64, true>(a, num_sms, stream) : launch_bwd_t<64, false>(a, num_sms, stream);
   return a.causal ? launch_bwd_t<128, true>(a, num_sms, stream) : launch_bwd_t<128, false>(a, num_sms, stream);

@@ -28,18 +28,20 @@ struct FwdArgs {
 };
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (loads)
-  CUtensorMap tm_dq, tm_dk, tm_dv;      // bf16 [BH][N][d], box 64 x 128 x 1, 128B swizzle (stores)
-  const void* o;                        // bf16 [BH][N][d]
-  const void* dO;                       // bf16 [BH][N][d]
-  const float* lse;                     // fp32 [BH][N]
-  float* Dsum;                          // fp32 [BH][N], in the caller's workspace
+  // bf16, box 64 x 128 x 1, 128B swizzle: q, dO, dq over [BH][Nq][d]; k, v, dk, dv over [BH][Nk][d]
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
+  CUtensorMap tm_dq, tm_dk, tm_dv;      // stores
+  const void* o;                        // bf16 [BH][Nq][d]
+  const void* dO;                       // bf16 [BH][Nq][d]
+  const float* lse;                     // fp32 [BH][Nq]
+  float* Dsum;                          // fp32 [BH][Nq], in the caller's workspace
   unsigned int* work;                   // work counters in the caller's workspace ([0] dK/dV, [1] dQ)
   unsigned int* status;
-  int BH, N, d;
+  int BH, Nq, Nk, d;
   float scale, scale_log2;
-  int causal;
-  int head_group;  // heads per CTA scheduling group (set by launch_bwd)
+  int causal;         // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
+  int head_group;     // heads per CTA scheduling group of the dK/dV kernel (set by launch_bwd)
+  int head_group_dq;  // the same for the dQ kernel
 };
 
 // Heads per CTA scheduling group for a (BH x nblk) grid whose causal CTAs

@@ -2,11 +2,12 @@
 
 Argument marshalling only: every step of attention runs in the CUDA kernels
 of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
-``fa_fwd_kv_workspace_bytes``, ``fa_bwd``, ``fa_bwd_workspace_bytes``,
+``fa_fwd_kv_workspace_bytes``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
+``fa_bwd_kv_workspace_bytes``,
 ``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
 torch CUDA tensors or raw device addresses (ints). ``forward``,
-``forward_kv`` and ``backward`` are conveniences that allocate the outputs
-with torch.
+``forward_kv``, ``backward`` and ``backward_kv`` are conveniences that
+allocate the outputs with torch.
 
 If the library has not been built, or cannot be loaded, every call raises:
 there is no fallback implementation.
@@ -28,8 +29,8 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_status_string",
-            "fa_device_status", "fa_bwd_noalloc")
+EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_kv",
+            "fa_bwd_kv_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +67,11 @@ def load(path: str | None = None):
         lib.fa_fwd_kv.restype = c_int
         lib.fa_fwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
         lib.fa_fwd_kv_workspace_bytes.restype = c_size_t
+        lib.fa_bwd_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                  vp, c_size_t, vp]
+        lib.fa_bwd_kv.restype = c_int
+        lib.fa_bwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
+        lib.fa_bwd_kv_workspace_bytes.restype = c_size_t
         lib.fa_bwd_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
         lib.fa_bwd_workspace_bytes.restype = c_size_t
         lib.fa_status_string.argtypes = [c_int]
@@ -128,6 +134,17 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, N: int, d: int, scal
                              int(workspace_bytes), _stream(stream)))
 
 
+def fa_bwd_kv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: bool,
+              workspace, workspace_bytes: int, stream=None) -> int:
+    return int(load().fa_bwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dO), _addr(dq), _addr(dk),
+                                _addr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)), _addr(workspace),
+                                int(workspace_bytes), _stream(stream)))
+
+
 def fa_device_status(reset: bool = True) -> int:
     return int(load().fa_device_status(int(bool(reset))))
 
@@ -184,6 +201,22 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
                 workspace.numel() * workspace.element_size(), stream)
     if st != FA_OK:
         raise FAError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def backward_kv(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None):
+    """Nq query rows against Nk keys: allocate dq, dk, dv and the workspace with torch and run fa_bwd_kv."""
+    import torch
+
+    B, H, Nq, d = _shape(q)
+    Nk = int(k.shape[2])
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, ws, need, stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_kv")
     return dq, dk, dv
 
 

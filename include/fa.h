@@ -137,6 +137,20 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
            size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd for Nq query rows against Nk keys (the backward of fa_fwd_kv, with
+ * the same causal rule: key j visible to query i iff j <= i + Nk - Nq, which
+ * needs Nq <= Nk). q, o, dO, dq are [B, H, Nq, d]; k, v, dk, dv [B, H, Nk, d];
+ * lse [B, H, Nq] (the logsumexp fa_fwd_kv returned). The workspace holds D
+ * for the Nq rows and the work counters: fa_bwd_kv_workspace_bytes bytes,
+ * 256-byte aligned. fa_bwd(..., N, ...) is fa_bwd_kv(..., N, N, ...).
+ * Returns FA_OK or an fa_status error code.
+ */
+FA_API size_t fa_bwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+FA_API int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Largest scratch, in bytes, that fa_bwd_noalloc holds per device: the
  * shapes it accepts are those with fa_bwd_workspace_bytes(B, H, N, d) <= this
  * (B * H * N up to 8,388,544 rows).

@@ -117,6 +117,31 @@ def test_bwd_rejects_bad_args(lib, args, status):
     assert st == status
 
 
+@pytest.mark.parametrize("args,status", [
+    (dict(dk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=1, Nq=80, Nk=64), fa.FA_ERR_INVALID_ARG),
+    (dict(d=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(dv=A + 4), fa.FA_ERR_MISALIGNED),
+    (dict(ws_bytes=16), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_kv_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=16, Nk=64, d=64, scale=0.125, causal=1,
+              ws=A, ws_bytes=1 << 20)
+    kw.update(args)
+    st = fa.fa_bwd_kv(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["dO"], kw["dq"], kw["dk"], kw["dv"], kw["B"],
+                      kw["H"], kw["Nq"], kw["Nk"], kw["d"], kw["scale"], kw["causal"], kw["ws"], kw["ws_bytes"],
+                      stream=0)
+    assert st == status
+
+
+def test_bwd_kv_workspace_bytes(lib):
+    # fp32 D for the Nq query rows, padded to 256 bytes, then 256 bytes of work counters
+    assert fa.fa_bwd_kv_workspace_bytes(2, 3, 100, 5000, 64) == ((2 * 3 * 100 * 4 + 255) // 256) * 256 + 256
+    assert fa.fa_bwd_kv_workspace_bytes(2, 3, 100, 100, 64) == fa.fa_bwd_workspace_bytes(2, 3, 100, 64)
+    assert fa.fa_bwd_kv_workspace_bytes(1, 1, 4, 0, 64) == 0
+
+
 def test_no_gpu_reports_launch_error(lib):
     import torch
 
