@@ -24,6 +24,13 @@
  * this is the reading under which Nq = Nk gives the mask above). Causal needs
  * Nq <= Nk, so that every row sees at least one key.
  *
+ * Both _kv functions optionally take per-head sequence lengths sq[h] <= Nq and
+ * sk[h] <= Nk (padding masks): head h then has only its first sq[h] query
+ * rows and sk[h] keys, with the causal rule above written for those lengths
+ * (row i sees keys 0..i + sk - sq). Padding rows get o = 0 and lse = -inf in
+ * the forward and dq = 0, D = 0 in the backward; padding keys get dk = dv = 0
+ * and are seen by no row.
+ *
  * Forward, per head and row i (chapter 08 defines the row max m and the sum
  * of exponentials l that the tiled method carries; here they are taken over
  * the whole row at once):
@@ -87,10 +94,19 @@ static void score_row(const double* qi, const double* k, int n, int d, double sc
  * and lse entries elsewhere are left untouched). Returns 0, or -1 on a bad
  * argument (including causal with Nq > Nk) or allocation failure.
  */
+static int bad_lengths(int BH, int Nq, int Nk, int causal, const int* sq, const int* sk) {
+  for (int h = 0; h < BH; ++h) {
+    const int a = sq ? sq[h] : Nq, b = sk ? sk[h] : Nk;
+    if (a < 1 || a > Nq || b < 1 || b > Nk || (causal && a > b)) return 1;
+  }
+  return 0;
+}
+
 int oracle_fwd_kv(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int Nq, int Nk,
-                  int d, double scale, int causal, const int* rows, int nrows, int nthreads) {
+                  int d, double scale, int causal, const int* sq, const int* sk, const int* rows, int nrows,
+                  int nthreads) {
   if (BH < 1 || Nq < 1 || Nk < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
-  if (causal && Nq > Nk) return -1;
+  if (bad_lengths(BH, Nq, Nk, causal, sq, sk)) return -1;
   if (!rows) nrows = Nq;
   for (int r = 0; rows && r < nrows; ++r)
     if (rows[r] < 0 || rows[r] >= Nq) return -1;
@@ -112,11 +128,16 @@ int oracle_fwd_kv(const double* q, const double* k, const double* v, double* o, 
       const double* qi = q + ((size_t)h * Nq + i) * d;
       const double* kh = k + (size_t)h * Nk * d;
       const double* vh = v + (size_t)h * Nk * d;
-      const int n = row_len_kv(i, Nq, Nk, causal);
-      double M, l;
-      score_row(qi, kh, n, d, scale, s, &M, &l);
+      const int a = sq ? sq[h] : Nq, b = sk ? sk[h] : Nk;
       double* oi = o + ((size_t)h * Nq + i) * d;
       for (int t = 0; t < d; ++t) oi[t] = 0.0;
+      if (i >= a) { /* a padding row */
+        lse[(size_t)h * Nq + i] = -INFINITY;
+        continue;
+      }
+      const int n = row_len_kv(i, a, b, causal);
+      double M, l;
+      score_row(qi, kh, n, d, scale, s, &M, &l);
       for (int j = 0; j < n; ++j) {
         const double p = exp(s[j] - M) / l;
         const double* vj = vh + (size_t)j * d;
@@ -132,7 +153,7 @@ int oracle_fwd_kv(const double* q, const double* k, const double* v, double* o, 
 /* Forward pass of self-attention (Nq = Nk = N): the listed rows, or all. */
 int oracle_fwd(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int N, int d,
                double scale, int causal, const int* rows, int nrows, int nthreads) {
-  return oracle_fwd_kv(q, k, v, o, lse, BH, N, N, d, scale, causal, rows, nrows, nthreads);
+  return oracle_fwd_kv(q, k, v, o, lse, BH, N, N, d, scale, causal, NULL, NULL, rows, nrows, nthreads);
 }
 
 /*
@@ -143,11 +164,10 @@ int oracle_fwd(const double* q, const double* k, const double* v, double* o, dou
  * keys). D, if non-NULL, receives D_i for every row. Returns 0, or -1 on error.
  */
 int oracle_bwd_kv(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
-                  double* dv, double* D, int BH, int Nq, int Nk, int d, double scale, int causal, const int* qrows,
-                  int nqr, const int* keys, int nkr, int nthreads) {
+                  double* dv, double* D, int BH, int Nq, int Nk, int d, double scale, int causal, const int* sq,
+                  const int* sk, const int* qrows, int nqr, const int* keys, int nkr, int nthreads) {
   if (BH < 1 || Nq < 1 || Nk < 1 || d < 1 || !q || !k || !v || !dO || !dq || !dk || !dv) return -1;
-  if (causal && Nq > Nk) return -1;
-  const int off = Nk - Nq;
+  if (bad_lengths(BH, Nq, Nk, causal, sq, sk)) return -1;
   if (!qrows) nqr = Nq;
   if (!keys) nkr = Nk;
   for (int r = 0; qrows && r < nqr; ++r)
@@ -184,7 +204,15 @@ int oracle_bwd_kv(const double* q, const double* k, const double* v, const doubl
       const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nk * d;
       const double* qi = q + qb + (size_t)i * d;
       const double* dOi = dO + qb + (size_t)i * d;
-      const int n = row_len_kv(i, Nq, Nk, causal);
+      const int a = sq ? sq[h] : Nq, b = sk ? sk[h] : Nk;
+      if (i >= a) { /* a padding row: no gradient, and it sees no key */
+        lse_all[w] = INFINITY;
+        D_all[w] = 0.0;
+        if (want_q[i])
+          for (int t = 0; t < d; ++t) dq[qb + (size_t)i * d + t] = 0.0;
+        continue;
+      }
+      const int n = row_len_kv(i, a, b, causal);
       double M, l;
       score_row(qi, k + kb, n, d, scale, s, &M, &l);
       double Di = 0.0;
@@ -225,7 +253,9 @@ int oracle_bwd_kv(const double* q, const double* k, const double* v, const doubl
         dkj[t] = 0.0;
         dvj[t] = 0.0;
       }
-      for (int i = causal && j > off ? j - off : 0; i < Nq; ++i) {
+      const int a = sq ? sq[h] : Nq, b = sk ? sk[h] : Nk, off = b - a;
+      if (j >= b) continue; /* a padding key */
+      for (int i = causal && j > off ? j - off : 0; i < a; ++i) {
         const double* qi = q + qb + (size_t)i * d;
         const double* dOi = dO + qb + (size_t)i * d;
         const double p = exp(scale * dot(qi, kj, d) - lse_all[(size_t)h * Nq + i]);
@@ -248,7 +278,8 @@ int oracle_bwd_kv(const double* q, const double* k, const double* v, const doubl
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
                double* dv, double* D, int BH, int N, int d, double scale, int causal, const int* qrows, int nq,
                const int* keys, int nk, int nthreads) {
-  return oracle_bwd_kv(q, k, v, dO, dq, dk, dv, D, BH, N, N, d, scale, causal, qrows, nq, keys, nk, nthreads);
+  return oracle_bwd_kv(q, k, v, dO, dq, dk, dv, D, BH, N, N, d, scale, causal, NULL, NULL, qrows, nq, keys, nk,
+                       nthreads);
 }
 
 /* Number of threads an OpenMP parallel region would use (1 without OpenMP). */

@@ -66,14 +66,14 @@ def load(path: str | None = None):
         c_int, c_double = ctypes.c_int, ctypes.c_double
         lib.oracle_fwd.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, ip, c_int, c_int]
         lib.oracle_fwd.restype = c_int
-        lib.oracle_fwd_kv.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int, ip, c_int,
-                                      c_int]
+        lib.oracle_fwd_kv.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int, ip, ip, ip,
+                                      c_int, c_int]
         lib.oracle_fwd_kv.restype = c_int
         lib.oracle_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int,
                                    ip, c_int, ip, c_int, c_int]
         lib.oracle_bwd.restype = c_int
         lib.oracle_bwd_kv.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int,
-                                      ip, c_int, ip, c_int, c_int]
+                                      ip, ip, ip, c_int, ip, c_int, c_int]
         lib.oracle_bwd_kv.restype = c_int
         lib.oracle_max_threads.argtypes = [c_int]
         lib.oracle_max_threads.restype = c_int
@@ -127,11 +127,22 @@ def fwd(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=N
     return o, lse
 
 
-def fwd_kv(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None):
+def _lens(x, BH):
+    if x is None:
+        return None, None
+    a = np.ascontiguousarray(np.broadcast_to(np.asarray(x, dtype=np.int32), (BH,)))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def fwd_kv(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, lib=None, seqlens_q=None,
+           seqlens_k=None):
     """O and lse for Nq query rows against Nk keys, fp64 (causal: row i sees keys <= i + Nk - Nq).
 
     ``rows`` (optional) restricts the computation to those query rows of every
-    head; the other rows of the returned arrays are NaN.
+    head; the other rows of the returned arrays are NaN. ``seqlens_q`` /
+    ``seqlens_k`` (optional, one per head) are padding masks: head h has only
+    its first seqlens_q[h] rows and seqlens_k[h] keys (causal: row i sees keys
+    <= i + seqlens_k - seqlens_q); padding rows get o = 0 and lse = -inf.
     """
     lib = lib or load()
     q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
@@ -142,9 +153,11 @@ def fwd_kv(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0, li
     o = np.full_like(q3, np.nan)
     lse = np.full((BH, Nq), np.nan)
     ridx, nr = _iptr(rows)
+    sq, sqp = _lens(seqlens_q, BH)
+    sk, skp = _lens(seqlens_k, BH)
     rc = lib.oracle_fwd_kv(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(o), _dptr(lse), BH, Nq, Nk, d, float(scale),
-                           int(causal), None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
-                           nr, nthreads)
+                           int(causal), sqp, skp,
+                           None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nr, nthreads)
     if rc != 0:
         raise RuntimeError("oracle_fwd_kv failed (causal needs Nq <= Nk)")
     return o, lse
@@ -175,7 +188,8 @@ def bwd(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads
     return dq, dk, dv, D
 
 
-def bwd_kv(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads: int = 0, lib=None):
+def bwd_kv(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthreads: int = 0, lib=None,
+           seqlens_q=None, seqlens_k=None):
     """dq [BH, Nq, d], dk and dv [BH, Nk, d] and D [BH, Nq] for Nq query rows against Nk keys, fp64
     (causal: row i sees keys <= i + Nk - Nq; needs Nq <= Nk). ``qrows`` / ``keys`` as in ``bwd``."""
     lib = lib or load()
@@ -188,9 +202,11 @@ def bwd_kv(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthre
     D = np.full((BH, Nq), np.nan)
     qi, nq = _iptr(qrows)
     ki, nk = _iptr(keys)
+    sq, sqp = _lens(seqlens_q, BH)
+    sk, skp = _lens(seqlens_k, BH)
     ip = ctypes.POINTER(ctypes.c_int)
     rc = lib.oracle_bwd_kv(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(dO3), _dptr(dq), _dptr(dk), _dptr(dv), _dptr(D),
-                           BH, Nq, Nk, d, float(scale), int(causal),
+                           BH, Nq, Nk, d, float(scale), int(causal), sqp, skp,
                            None if qi is None else qi.ctypes.data_as(ip), nq,
                            None if ki is None else ki.ctypes.data_as(ip), nk, nthreads)
     if rc != 0:

@@ -331,6 +331,34 @@ def pin_kv_bwd_suffix_of_self_attention(lib=None):
         assert all(np.allclose(x, y, rtol=0, atol=1e-15) for x, y in zip(a, b))
 
 
+def pin_padding_lengths_are_truncation(lib=None):
+    """Per-head lengths (padding masks): each head's real rows and keys give exactly the result of the
+    truncated tensors; padding rows get o = 0, lse = -inf, dq = 0, D = 0; padding keys get dk = dv = 0."""
+    BH, Nq, Nk, d = 3, 9, 14, 8
+    q, k, v = _kv(170, BH, Nq, Nk, d)
+    dO = np.random.default_rng(171).standard_normal((BH, Nq, d))
+    sq, sk = np.array([9, 4, 1]), np.array([14, 10, 3])
+    for causal in (False, True):
+        o, lse = orc.fwd_kv(q, k, v, 0.5, causal, lib=lib, seqlens_q=sq, seqlens_k=sk)
+        dq, dk, dv, D = orc.bwd_kv(q, k, v, dO, 0.5, causal, lib=lib, seqlens_q=sq, seqlens_k=sk)
+        for h in range(BH):
+            a, b = sq[h], sk[h]
+            ot, lt = orc.fwd_kv(q[h:h + 1, :a], k[h:h + 1, :b], v[h:h + 1, :b], 0.5, causal, lib=lib)
+            assert np.allclose(o[h, :a], ot[0], rtol=0, atol=1e-14) and np.allclose(lse[h, :a], lt[0], atol=1e-14)
+            assert np.all(o[h, a:] == 0) and np.all(np.isneginf(lse[h, a:]))
+            gt = orc.bwd_kv(q[h:h + 1, :a], k[h:h + 1, :b], v[h:h + 1, :b], dO[h:h + 1, :a], 0.5, causal, lib=lib)
+            assert np.allclose(dq[h, :a], gt[0][0], rtol=0, atol=1e-13) and np.all(dq[h, a:] == 0)
+            assert np.allclose(dk[h, :b], gt[1][0], rtol=0, atol=1e-13) and np.all(dk[h, b:] == 0)
+            assert np.allclose(dv[h, :b], gt[2][0], rtol=0, atol=1e-13) and np.all(dv[h, b:] == 0)
+            assert np.allclose(D[h, :a], gt[3][0], rtol=0, atol=1e-13) and np.all(D[h, a:] == 0)
+    try:
+        orc.fwd_kv(q, k, v, 0.5, True, lib=lib, seqlens_q=np.array([5, 5, 5]), seqlens_k=np.array([4, 9, 9]))
+    except RuntimeError:
+        pass
+    else:
+        raise AssertionError("causal with more query rows than keys in a head must be refused")
+
+
 ALL_PINS = [
     pin_zero_q_noncausal,
     pin_zero_q_causal,
@@ -351,4 +379,5 @@ ALL_PINS = [
     pin_kv_merge_of_key_ranges,
     pin_kv_bwd_torch_autograd,
     pin_kv_bwd_suffix_of_self_attention,
+    pin_padding_lengths_are_truncation,
 ]

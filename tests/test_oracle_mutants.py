@@ -20,16 +20,18 @@ MUTANTS = [
     ("output_reads_k_not_v", "const double* vh = v + (size_t)h * Nk * d;", "const double* vh = k + (size_t)h * Nk * d;"),
     ("kv_causal_top_left", "return causal ? i + 1 + (Nk - Nq) : Nk;", "return causal ? i + 1 : Nk;"),
     ("kv_query_head_stride", "const double* qi = q + ((size_t)h * Nq + i) * d;", "const double* qi = q + ((size_t)h * Nk + i) * d;"),
+    ("padding_row_off_by_one", "if (i >= a) { /* a padding row */", "if (i > a) { /* a padding row */"),
+    ("padding_key_ignored", "if (j >= b) continue; /* a padding key */", "if (j >= Nk) continue; /* a padding key */"),
     ("bwd_kv_key_head_stride", "const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nk * d;\n      const double* kj",
      "const size_t qb = (size_t)h * Nq * d, kb = (size_t)h * Nq * d;\n      const double* kj"),
     ("D_wrong_sign", "Di += s[j] * dp[j];", "Di -= s[j] * dp[j];"),
     ("dq_dropped_scale", "dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
     ("dk_transposed_operand", "dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
     ("dv_uses_dS", "dvj[t] += p * dOi[t];", "dvj[t] += ds * dOi[t];"),
-    ("bwd_causal_skips_diagonal", "for (int i = causal && j > off ? j - off : 0; i < Nq; ++i)",
-     "for (int i = causal && j >= off ? j - off + 1 : 0; i < Nq; ++i)"),
-    ("bwd_mask_reversed", "for (int i = causal && j > off ? j - off : 0; i < Nq; ++i)",
-     "for (int i = 0; i < (causal ? (j - off + 1 > 0 ? j - off + 1 : 0) : Nq) && i < Nq; ++i)"),
+    ("bwd_causal_skips_diagonal", "for (int i = causal && j > off ? j - off : 0; i < a; ++i)",
+     "for (int i = causal && j >= off ? j - off + 1 : 0; i < a; ++i)"),
+    ("bwd_mask_reversed", "for (int i = causal && j > off ? j - off : 0; i < a; ++i)",
+     "for (int i = 0; i < (causal ? (j - off + 1 > 0 ? j - off + 1 : 0) : a) && i < a; ++i)"),
     ("dp_uses_o_index", "dp[j] = dot(dOi, v + kb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + kb + (size_t)i * d, d);"),
 ]
 
