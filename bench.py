@@ -464,8 +464,8 @@ def run_decode(args, c):
     sp = int(stream.cuda_stream)
 
     def call(xq=q, xo=o, xlse=lse):
-        st = fa.fa_fwd_kv(xq, k, v, xo, xlse, B, H, Nq, Nk, d, scale, causal, ws if ws_bytes else None, ws_bytes,
-                          sp)
+        st = fa.fa_fwd_kv(xq, k, v, xo, xlse, B, H, Nq, Nk, d, scale, causal, None, None,
+                          ws if ws_bytes else None, ws_bytes, sp)
         if st:
             raise fa.FAError(st, "fa_fwd_kv")
 

@@ -67,6 +67,7 @@ int device_info(DeviceInfo** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const int* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }  // (NULL passes)
 
 int check_shape(int B, int H, int N, int d, float scale) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
@@ -101,7 +102,7 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, void* stream) {
-  return fa_fwd_kv(q, k, v, o, lse, B, H, N, N, d, scale, causal, nullptr, 0, stream);
+  return fa_fwd_kv(q, k, v, o, lse, B, H, N, N, d, scale, causal, nullptr, nullptr, nullptr, 0, stream);
 }
 
 size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -115,14 +116,15 @@ size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
 }
 
 int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-              float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+              float scale, int causal, const int* seqlens_q, const int* seqlens_k, void* workspace,
+              size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int st = check_shape(B, H, Nq, d, scale);
   if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
   if (st != FA_OK) return st;
   if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (workspace && !aligned16(workspace)))
+      (workspace && !aligned16(workspace)) || !aligned4(seqlens_q) || !aligned4(seqlens_k))
     return FA_ERR_MISALIGNED;
   DeviceInfo* di = nullptr;
   if ((st = device_info(&di)) != FA_OK) return st;
@@ -138,11 +140,14 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.lse = lse;
   a.status = di->status;
   a.BH = BH;
+  a.H = H;
   a.Nq = Nq;
   a.Nk = Nk;
   a.d = d;
   a.scale_log2 = (float)((double)scale * kLog2e);
   a.causal = causal ? 1 : 0;
+  a.seqlens_q = seqlens_q;
+  a.seqlens_k = seqlens_k;
   // Key ranges: as many as help fill the GPU and fit the caller's workspace
   // (none without one); every range non-empty.
   const int nkv = (Nk + 127) / 128;
@@ -172,19 +177,20 @@ size_t fa_bwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
            size_t workspace_bytes, void* stream) {
-  return fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, workspace, workspace_bytes, stream);
+  return fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, nullptr, nullptr, workspace,
+                   workspace_bytes, stream);
 }
 
 int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-              void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* workspace,
-              size_t workspace_bytes, void* stream) {
+              void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              const int* seqlens_q, const int* seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int st = check_shape(B, H, Nq, d, scale);
   if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
   if (st != FA_OK) return st;
   if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(seqlens_q) || !aligned4(seqlens_k))
     return FA_ERR_MISALIGNED;
   const size_t need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -209,12 +215,15 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const 
   a.lse = lse;
   a.status = di->status;
   a.BH = BH;
+  a.H = H;
   a.Nq = Nq;
   a.Nk = Nk;
   a.d = d;
   a.scale = scale;
   a.scale_log2 = (float)((double)scale * kLog2e);
   a.causal = causal ? 1 : 0;
+  a.seqlens_q = seqlens_q;
+  a.seqlens_k = seqlens_k;
   return fa::launch_bwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -242,7 +251,8 @@ int fa_device_status(int reset) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_fa_device_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_LAUNCH;
   }
-  return word ? FA_ERR_TIMEOUT : FA_OK;
+  if (word & ~fa::kStatusBadLength) return FA_ERR_TIMEOUT;
+  return word ? FA_ERR_INVALID_ARG : FA_OK;
 }
 
 }  // extern "C"

@@ -148,24 +148,35 @@ __device__ __forceinline__ uint32_t dkdv_pcol(int kk, bool ds) {
 // k-step of the i-th of the four 16-query steps in query half h: {0, 1, 4, 5} or {2, 3, 6, 7}.
 __device__ __forceinline__ constexpr int dkdv_half_kstep(int h, int i) { return 4 * (i >> 1) + 2 * h + (i & 1); }
 
-// A dK/dV tile: (head, key block), its first query block and how many it sees.
+// A dK/dV tile: (head, key block), its first query block and how many it
+// sees, and the sequence's query rows sq and keys sk (padding masks).
 struct DkdvTile {
-  int bh, kblk, i_start, n;
+  int bh, kblk, i_start, n, sq, sk;
 };
 
-template <bool CAUSAL>
-__device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nq, int nkv) {
+// VARLEN: per-sequence lengths are given (padding masks); without them the
+// lengths are the array sizes, which the kernels then take as constants.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nkv) {
   DkdvTile t;
   grouped_index(L, a.BH, nkv, a.head_group, t.bh, t.kblk);  // key block 0 (the heaviest) first
-  // BQ == BK: query block i sees key block j iff its last row does, 128 i + 127 + Nk - Nq >= 128 j
-  // (with Nq = Nk: iff i >= j). The last query row sees every key, so n >= 1.
-  const int x = t.kblk * 128 - 127 - (a.Nk - a.Nq);
+  t.sq = a.Nq;
+  t.sk = a.Nk;
+  if (VARLEN) seq_lens(a.seqlens_q, a.seqlens_k, t.bh / a.H, a.Nq, a.Nk, CAUSAL, t.sq, t.sk);
+  if (VARLEN && t.kblk * 128 >= t.sk) {  // padding keys only: one fully masked block gives dk = dv = 0
+    t.i_start = 0;
+    t.n = 1;
+    return t;
+  }
+  // BQ == BK: query block i sees key block j iff its last row does, 128 i + 127 + sk - sq >= 128 j
+  // (with sq = sk: iff i >= j). The last query row sees every key, so n >= 1.
+  const int x = t.kblk * 128 - 127 - (t.sk - t.sq);
   t.i_start = CAUSAL && x > 0 ? (x + 127) / 128 : 0;
-  t.n = nq - t.i_start;
+  t.n = (t.sq + 127) / 128 - t.i_start;
   return t;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -179,10 +190,8 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
   float* rowbuf = reinterpret_cast<float*>(smem + C::kOffRow);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Nq = a.Nq, Nk = a.Nk;
-  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
-  const int nq = (Nq + C::BQ - 1) / C::BQ;
-  const int nkv = (Nk + C::BK - 1) / C::BK;
+  const int Nq = a.Nq;  // rows of the q / lse / D arrays
+  const int nkv = (a.Nk + C::BK - 1) / C::BK;
   const int total = a.BH * nkv;
 
   if (threadIdx.x == 0) {
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
       if (L >= total) break;
-      const DkdvTile t = dkdv_tile<CAUSAL>(L, a, nq, nkv);
+      const DkdvTile t = dkdv_tile<CAUSAL, VARLEN>(L, a, nkv);
       bars.st_bh[k & 7] = t.bh;  // every lane writes the same values
       bars.st_kblk[k & 7] = t.kblk;
       bars.st_last[k & 7] = g + t.n - 1;
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
           tiles_done = true;
           return Blk{0, 0, -1};
         }
-        cursor = Blk{0, dkdv_tile<CAUSAL>(L, a, nq, nkv).n, cursor.kt + 1};
+        cursor = Blk{0, dkdv_tile<CAUSAL, VARLEN>(L, a, nkv).n, cursor.kt + 1};
         return cursor;
       };
       if (warp == 10) {
@@ -545,23 +554,26 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
     // later, so that no thread waits for the load in between.
     auto fetch = [&](const DkdvTile& t, int qb) -> float {
       const int q = qb * C::BQ + 64 * w + (tt & 63);
-      if (tt < 64) return q < Nq ? a.lse[(size_t)t.bh * Nq + q] : INFINITY;  // 2^(x - inf) = 0 past Nq
-      return q < Nq ? a.Dsum[(size_t)t.bh * Nq + q] : 0.f;
+      const int sq = VARLEN ? t.sq : Nq;
+      if (tt < 64) return q < sq ? a.lse[(size_t)t.bh * Nq + q] : INFINITY;  // 2^(x - inf) = 0 past sq
+      return q < sq ? a.Dsum[(size_t)t.bh * Nq + q] : 0.f;
     };
     // After a failed wait a warp keeps going without work; at every block the
     // group's named barrier also ANDs the warps' states, so the four warps
     // always agree on their blocks and tiles and meet at the same barriers.
     int L = take_tile(0);
-    DkdvTile t = L >= 0 ? dkdv_tile<CAUSAL>(L, a, nq, nkv) : DkdvTile{0, 0, 0, 0};
+    DkdvTile t = L >= 0 ? dkdv_tile<CAUSAL, VARLEN>(L, a, nkv) : DkdvTile{0, 0, 0, 0, 1, 1};
     float next = L >= 0 ? fetch(t, t.i_start) : 0.f;
     bool ok = L >= 0;
     int g = 0;
     for (int k = 0; L >= 0; ++k) {
       const int key = t.kblk * C::BK + r;
-      const bool key_ok = key < Nk;
-      const bool keys_all_ok = (t.kblk + 1) * C::BK <= Nk;  // uniform over the CTA
+      const int sk = VARLEN ? t.sk : a.Nk;
+      const bool key_ok = key < sk;
+      const bool keys_all_ok = (t.kblk + 1) * C::BK <= sk;  // uniform over the CTA
+      const int off = sk - (VARLEN ? t.sq : Nq);  // causal: query row i sees keys 0 .. i + off
       int L_next = -1;
-      DkdvTile nt = {0, 0, 0, 0};
+      DkdvTile nt = {0, 0, 0, 0, 1, 1};
       for (int it = 0; it < t.n; ++it, ++g) {
         const int q0 = (t.i_start + it) * C::BQ;
         float* rb = rowbuf + ((g & 1) * 2 + w) * 128;
@@ -572,7 +584,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
         } else {  // the next tile's first block
           L_next = take_tile(k + 1);
           if (L_next >= 0) {
-            nt = dkdv_tile<CAUSAL>(L_next, a, nq, nkv);
+            nt = dkdv_tile<CAUSAL, VARLEN>(L_next, a, nkv);
             next = fetch(nt, nt.i_start);
           }
         }
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
           mbar_arrive(&bars.s_free);  // S^T is in registers: the next block's S^T may overwrite it
           // Only blocks whose first query row does not see the block's last key
           // (the diagonal, the first block under the causal mask; a second one when
-          // Nk - Nq is not a multiple of 128) and a ragged last key block need
+          // sk - sq is not a multiple of 128) and a ragged last key block need
           // masking: there a hidden score becomes -inf, so P = 0 (scale > 0).
           // Query q0 + 64 w + col sees key kblk * BK + r iff q0 + 64 w + col + off >= key.
           if ((CAUSAL && q0 + off < (t.kblk + 1) * C::BK - 1) || !keys_all_ok) {
@@ -752,22 +764,29 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
 }
 
 // A dQ tile: (head, query block) and the number of key blocks it sees.
+// A dQ tile: (head, query block), the key blocks it sees, and the sequence's
+// query rows sq and keys sk (padding masks).
 struct DqTile {
-  int bh, qblk, nk;
+  int bh, qblk, nk, sq, sk;
 };
 
-template <bool CAUSAL>
-__device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq, int nkv) {
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq) {
   DqTile t;
   int blk;
   grouped_index(L, a.BH, nq, a.head_group_dq, t.bh, blk);
   t.qblk = CAUSAL ? nq - 1 - blk : blk;  // heaviest first under the causal mask
-  // BQ == BK: query block i sees key blocks 0 .. (128 i + 127 + Nk - Nq) / 128 (with Nq = Nk: 0..i)
-  t.nk = CAUSAL ? min((t.qblk * 128 + 127 + a.Nk - a.Nq) / 128 + 1, nkv) : nkv;
+  t.sq = a.Nq;
+  t.sk = a.Nk;
+  if (VARLEN) seq_lens(a.seqlens_q, a.seqlens_k, t.bh / a.H, a.Nq, a.Nk, CAUSAL, t.sq, t.sk);
+  const int nkv = (t.sk + 127) / 128;
+  // BQ == BK: query block i sees key blocks 0 .. (128 i + 127 + sk - sq) / 128 (with sq = sk: 0..i);
+  // a block of padding rows only takes one key block, whose P = 0 gives dq = 0
+  t.nk = VARLEN && t.qblk * 128 >= t.sq ? 1 : CAUSAL ? min((t.qblk * 128 + 127 + t.sk - t.sq) / 128 + 1, nkv) : nkv;
   return t;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -776,10 +795,8 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
   volatile int* abort_flag = &bars.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Nq = a.Nq, Nk = a.Nk;
-  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
+  const int Nq = a.Nq;  // rows of the q / lse / D arrays
   const int nq = (Nq + C::BQ - 1) / C::BQ;
-  const int nkv = (Nk + C::BK - 1) / C::BK;
   const int total = a.BH * nq;
 
   if (threadIdx.x == 0) {
@@ -885,7 +902,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_full[is]);  // release: the tile index is visible
       if (L >= total) break;
-      const DqTile t = dq_tile<CAUSAL>(L, a, nq, nkv);
+      const DqTile t = dq_tile<CAUSAL, VARLEN>(L, a, nq);
       if (k == 1 && !(ok = warp_wait(&bars.qt_ready, 0, abort_flag))) break;
       if (k >= 2 && !(ok = store_dq(k - 2, false))) break;
       if (k & 1)
@@ -966,7 +983,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
         int k = 0, g = 0;  // tile and key block over the CTA's run
         bool ok = true;
         for (int L = take_tile(0); ok && L >= 0; L = take_tile(++k)) {
-          const DqTile t = dq_tile<CAUSAL>(L, a, nq, nkv);
+          const DqTile t = dq_tile<CAUSAL, VARLEN>(L, a, nq);
           for (int j = 0; j < t.nk; ++j) {
             const int gj = g + j;
             if (!(ok = warp_wait2(&bars.ds_ready, gj & 1, &bars.k_full[gj % C::kKStages], k_phase(gj), abort_flag)))
@@ -1019,7 +1036,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
         };
         int k = 0, g = 0;  // tile and key block over the CTA's run
         int L = take_tile(0);
-        DqTile t = L >= 0 ? dq_tile<CAUSAL>(L, a, nq, nkv) : DqTile{0, 0, 0};
+        DqTile t = L >= 0 ? dq_tile<CAUSAL, VARLEN>(L, a, nq) : DqTile{0, 0, 0, 1, 1};
         bool ok = L >= 0;
         while (ok) {
           // the tile's first block: S needs its Q in TMEM (the warpgroups copy it
@@ -1050,7 +1067,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
           g += t.nk;
           ++k;
           if ((L = take_tile(k)) < 0) break;
-          t = dq_tile<CAUSAL>(L, a, nq, nkv);
+          t = dq_tile<CAUSAL, VARLEN>(L, a, nq);
         }
         if (elect_one()) mma_commit(&bars.teardown);  // the same lane as above: elect.sync picks the lowest
         __syncwarp();
@@ -1067,14 +1084,14 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     const uint32_t t_dp = tmem + lane_off + C::kColDP + 64 * w;
     const uint32_t t_ds = tmem + lane_off + C::kColDS + 32 * w;
     // this thread's row terms for a tile, loaded early and converted when
-    // the tile starts (rows past Nq read row Nq - 1 and get P = 0 then)
+    // the tile starts (rows past sq get P = 0 then; rows past Nq read row Nq - 1)
     auto load_row_terms = [&](const DqTile& t, float& lse_raw, float& d_raw) {
       const int q = min(t.qblk * C::BQ + r, Nq - 1);
       lse_raw = a.lse[(size_t)t.bh * Nq + q];
       d_raw = a.Dsum[(size_t)t.bh * Nq + q];
     };
     auto row_terms = [&](const DqTile& t, float lse_raw, float d_raw, float& lse2, float& dsum) {
-      const bool in = t.qblk * C::BQ + r < Nq;
+      const bool in = t.qblk * C::BQ + r < (VARLEN ? t.sq : Nq);
       lse2 = in ? lse_raw * kLog2e : INFINITY;
       dsum = in ? d_raw : 0.f;
     };
@@ -1095,7 +1112,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     int k = 0, g = 0;
     int L = take_tile(0);
     bool ok = L >= 0;
-    DqTile t = ok ? dq_tile<CAUSAL>(L, a, nq, nkv) : DqTile{0, 0, 0};
+    DqTile t = ok ? dq_tile<CAUSAL, VARLEN>(L, a, nq) : DqTile{0, 0, 0, 1, 1};
     float lse2 = 0.f, dsum = 0.f;
     if (ok) {
       float lr, dr;
@@ -1124,11 +1141,13 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
           tc_fence_before();
           mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
           // Only blocks reaching past the tile's first row's last key (the diagonal,
-          // or two blocks when Nk - Nq is not a multiple of 128) and a ragged last
-          // key block need masking: keys past the causal limit or past Nk get a
+          // or two blocks when sk - sq is not a multiple of 128) and a ragged last
+          // key block need masking: keys past the causal limit or past sk get a
           // -inf score, so P = 0 (scale > 0).
-          if ((CAUSAL && (j + 1) * C::BK - 1 > t.qblk * C::BQ + off) || (j + 1) * C::BK > Nk) {
-            const int lim = (CAUSAL ? min(q + off, Nk - 1) : Nk - 1) - k0;  // keep key k0 + col iff col <= lim
+          const int sk = VARLEN ? t.sk : a.Nk;
+          const int off = sk - (VARLEN ? t.sq : Nq);  // causal: query row i sees keys 0 .. i + off
+          if ((CAUSAL && (j + 1) * C::BK - 1 > t.qblk * C::BQ + off) || (j + 1) * C::BK > sk) {
+            const int lim = (CAUSAL ? min(q + off, sk - 1) : sk - 1) - k0;  // keep key k0 + col iff col <= lim
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -1196,7 +1215,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
       DqTile nt = {0, 0, 0};
       float lse_next = 0.f, d_next = 0.f;
       if (L >= 0) {
-        nt = dq_tile<CAUSAL>(L, a, nq, nkv);
+        nt = dq_tile<CAUSAL, VARLEN>(L, a, nq);
         load_row_terms(nt, lse_next, d_next);
         ok = copy_q(k + 1);
       }
@@ -1253,6 +1272,13 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant_
   for (int off = kThreadsPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) a.Dsum[row] = acc;
   if (blockIdx.x == 0 && threadIdx.x < 2) a.work[threadIdx.x] = 0u;  // tile counters of the next two kernels
+  // one thread per sequence checks its lengths (the other kernels clamp them)
+  const long long seq_rows = (long long)a.H * a.Nq;
+  if ((a.seqlens_q || a.seqlens_k) && part == 0 && row < rows && row % seq_rows == 0) {
+    int sq, sk;
+    if (seq_lens(a.seqlens_q, a.seqlens_k, (int)(row / seq_rows), a.Nq, a.Nk, a.causal != 0, sq, sk))
+      atomicOr(a.status, kStatusBadLength);
+  }
 }
 
 template <int D, bool CAUSAL>
@@ -1262,7 +1288,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   fa_bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kv = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  const bool varlen = a.seqlens_q || a.seqlens_k;
+  auto kv = varlen ? fa_bwd_dkdv_kernel<D, CAUSAL, true> : fa_bwd_dkdv_kernel<D, CAUSAL, false>;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
@@ -1270,7 +1297,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   const long long kv_tiles = (long long)a.BH * ((a.Nk + 127) / 128), q_tiles = (long long)a.BH * ((a.Nq + 127) / 128);
   kv<<<(unsigned)std::min<long long>(kv_tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  auto kq = fa_bwd_dq_kernel<D, CAUSAL>;
+  auto kq = varlen ? fa_bwd_dq_kernel<D, CAUSAL, true> : fa_bwd_dq_kernel<D, CAUSAL, false>;
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;

@@ -68,7 +68,19 @@ struct FwdBarriers {
   int abort;
 };
 
-template <int D, bool CAUSAL>
+// o = 0 and lse = -inf for rows [r0, r0 + n) of head bh (padding rows that
+// no product touches), by threads tid of nthr with plain 16-byte stores.
+template <int D>
+__device__ inline void zero_rows(const FwdArgs& a, int bh, int r0, int n, int tid, int nthr) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks of a bf16 row
+  uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + ((size_t)bh * a.Nq + r0) * D * 2);
+  for (int i = tid; i < n * kChunks; i += nthr) o[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < n; i += nthr) a.lse[(size_t)bh * a.Nq + r0 + i] = -INFINITY;
+}
+
+// VARLEN: per-sequence lengths are given (padding masks); without them the
+// lengths are the array sizes, which the kernel then takes as constants.
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -77,12 +89,16 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   volatile int* abort_flag = &bars.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Nq = a.Nq, Nk = a.Nk;
-  const int off = Nk - Nq;  // causal: query row i sees keys 0 .. i + off
+  const int Nq = a.Nq;  // rows of the q / o / lse arrays
   int bh, blk;
   grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
   const int qblk = CAUSAL ? (int)gridDim.y - 1 - blk : blk;  // heaviest first under the causal mask
-  const int nkv = (Nk + C::BN - 1) / C::BN;
+  // this sequence's query rows sq and keys sk (all of them without padding masks)
+  int sq = Nq, sk = a.Nk;
+  if (VARLEN && seq_lens(a.seqlens_q, a.seqlens_k, bh / a.H, Nq, a.Nk, CAUSAL, sq, sk) && threadIdx.x == 0)
+    atomicOr(a.status, kStatusBadLength);
+  const int off = sk - sq;  // causal: query row i sees keys 0 .. i + off
+  const int nkv = (sk + C::BN - 1) / C::BN;
   // this CTA's key blocks: [jb, je) (all of them unless the keys are split)
   const int jb = (int)blockIdx.z * a.split_blocks;
   const int je = min(nkv, jb + a.split_blocks);
@@ -90,17 +106,23 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = qblk * 256 + t * 128;
-    const int last_key = CAUSAL ? min(min(r0 + 127, Nq - 1) + off, Nk - 1) : Nk - 1;
-    nb[t] = r0 < Nq ? max(0, min(last_key / C::BN + 1, je) - jb) : 0;
+    const int last_key = CAUSAL ? min(min(r0 + 127, sq - 1) + off, sk - 1) : sk - 1;
+    nb[t] = r0 < sq ? max(0, min(last_key / C::BN + 1, je) - jb) : 0;
   }
   const int nb_max = max(nb[0], nb[1]);
   if (nb_max == 0) {
-    // (key ranges only) no row of this CTA sees a key of its range: the range
-    // has no weight in the merge. The condition is uniform over the CTA, so
-    // every thread leaves before any barrier.
-    if (a.n_split > 1 && threadIdx.x < 256) {
-      const int row = qblk * 256 + (int)threadIdx.x;
-      if (row < Nq) a.lse_part[((size_t)blockIdx.z * a.BH + bh) * Nq + row] = -INFINITY;
+    // No row of this CTA sees a key of its range: either the keys are split
+    // and the range has no weight in the merge, or every row is padding
+    // (o = 0, lse = -inf). The condition is uniform over the CTA, so every
+    // thread leaves before any barrier.
+    if (a.n_split > 1) {
+      if (threadIdx.x < 256) {
+        const int row = qblk * 256 + (int)threadIdx.x;
+        if (row < Nq) a.lse_part[((size_t)blockIdx.z * a.BH + bh) * Nq + row] = -INFINITY;
+      }
+    } else if (VARLEN) {
+      const int r0 = qblk * 256;
+      zero_rows<D>(a, bh, r0, min(256, Nq - r0), (int)threadIdx.x, (int)blockDim.x);
     }
     return;
   }
@@ -307,12 +329,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
       // Only blocks that reach past the tile's first row's last key (the
-      // diagonal under the causal mask, one or two blocks) or past Nk need
+      // diagonal under the causal mask, one or two blocks) or past key sk - 1 need
       // masking: there a hidden score becomes -inf, so P = 0 (scale > 0).
       const int kv0 = (jb + j) * C::BN;
-      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > r0 + off) || kv0 + C::BN > Nk;
+      const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > r0 + off) || kv0 + C::BN > sk;
       if (need_mask) {
-        const int lim = (CAUSAL ? min(row + off, Nk - 1) : Nk - 1) - kv0;  // keep key column c iff c <= lim
+        const int lim = (CAUSAL ? min(row + off, sk - 1) : sk - 1) - kv0;  // keep key column c iff c <= lim
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
@@ -389,12 +411,17 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
                                                __uint_as_float(o[4 * i + 3]) * inv_l);
         }
       }
-      if (ok && row < Nq) a.lse_part[prow] = nbt > 0 && l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-    } else if (nbt > 0) {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
+      if (ok && row < Nq)
+        a.lse_part[prow] = nbt > 0 && l_sum > 0.f && (!VARLEN || row < sq) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    } else if (nbt == 0) {
+      // every row of this tile is padding (another tile of the CTA is not)
+      if (VARLEN && ok) zero_rows<D>(a, bh, r0, min(128, Nq - r0), r, 128);
+    } else {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
       uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is no longer read by any MMA
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l_sum;
+        const bool pad = VARLEN && row >= sq;  // a padding row among valid ones: o = 0
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
@@ -407,7 +434,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             const uint32_t addr = smem_u32(stage + pn * C::kPanelBytes + r * 128 + ((chunk ^ (r & 7)) << 4));
             float f[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(o[q4 * 8 + i]) * inv_l;
+            for (int i = 0; i < 8; ++i) f[i] = pad ? 0.f : __uint_as_float(o[q4 * 8 + i]) * inv_l;
             st_shared_v4(addr, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                          pack_bf16x2(f[6], f[7]));
           }
@@ -421,7 +448,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         bulk_commit();
         bulk_wait_read0();  // the staging tile has been read; the writes finish on their own
       }
-      if (ok && row < Nq) a.lse[(size_t)bh * Nq + row] = (m_ref + log2f(l_sum)) * kLn2;
+      if (ok && row < Nq)
+        a.lse[(size_t)bh * Nq + row] = !VARLEN || row < sq ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
     }
   }
 
@@ -435,8 +463,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 // m = max_z lse_z and w_z = e^(lse_z - m), o = sum_z w_z o_z / sum_z w_z and
 // lse = m + ln sum_z w_z (the running-maximum update of chapter 08 of
 // "FlashAttention and GPU Memory", for logsumexps, over all ranges at once).
-// A range the row sees no key of has lse_z = -inf and is skipped; every row
-// sees some key over all ranges, so m is finite.
+// A range the row sees no key of has lse_z = -inf and is skipped; a row with
+// no finite lse_z at all is a padding row: o = 0, lse = -inf.
 template <int D>
 __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int V = D / 32;  // values of the row per lane
@@ -459,20 +487,20 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const __grid_constant
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] += w * oz[i];
   }
-  const float inv = 1.f / tot;
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
   uint32_t packed[V / 2];
 #pragma unroll
   for (int i = 0; i < V / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
   uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.o) + (row * D + lane * V) * 2);
 #pragma unroll
   for (int i = 0; i < V / 2; ++i) dst[i] = packed[i];
-  if (lane == 0) a.lse[row] = m + logf(tot);
+  if (lane == 0) a.lse[row] = tot > 0.f ? m + logf(tot) : -INFINITY;
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = a.seqlens_q || a.seqlens_k ? fa_fwd_kernel<D, CAUSAL, true> : fa_fwd_kernel<D, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + 255) / 256), (unsigned)a.n_split);

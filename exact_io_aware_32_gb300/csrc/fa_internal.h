@@ -14,9 +14,13 @@ struct FwdArgs {
   void* o;                 // bf16 [BH][Nq][d] (written by the merge kernel when the keys are split)
   float* lse;              // fp32 [BH][Nq]
   unsigned int* status;    // device error word
-  int BH, Nq, Nk, d;
+  int BH, H, Nq, Nk, d;
   float scale_log2;  // scale * log2(e)
   int causal;        // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
+  // optional per-sequence lengths, int32 [B] (padding masks): batch b has only
+  // its first seq_len(seqlens_q, b, Nq) query rows and seq_len(seqlens_k, b, Nk) keys
+  const int* seqlens_q;
+  const int* seqlens_k;
   int head_group;    // heads per CTA scheduling group (set by launch_fwd)
   // Key ranges per query block. With n_split > 1, CTA z covers key blocks
   // [z * split_blocks, (z + 1) * split_blocks) and writes O / l (fp32) and the
@@ -37,12 +41,44 @@ struct BwdArgs {
   float* Dsum;                          // fp32 [BH][Nq], in the caller's workspace
   unsigned int* work;                   // work counters in the caller's workspace ([0] dK/dV, [1] dQ)
   unsigned int* status;
-  int BH, Nq, Nk, d;
+  int BH, H, Nq, Nk, d;
   float scale, scale_log2;
   int causal;         // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
+  const int* seqlens_q;  // optional per-sequence lengths, as in FwdArgs
+  const int* seqlens_k;
   int head_group;     // heads per CTA scheduling group of the dK/dV kernel (set by launch_bwd)
   int head_group_dq;  // the same for the dQ kernel
 };
+
+// Status bit a kernel sets when a per-sequence length lies outside [1, N]
+// (or, under the causal mask, a query length exceeds its key length); the
+// kernel then works with the length clamped into range.
+constexpr unsigned int kStatusBadLength = 32u;
+
+// Lengths of sequence b under the padding masks: sq query rows and sk keys,
+// each lens[b] clamped to [1, N] (N without lengths), and under the causal
+// mask sq cut to sk, so that every valid row sees a key. Returns true when a
+// length had to be changed.
+__device__ inline bool seq_lens(const int* lq, const int* lk, int b, int Nq, int Nk, bool causal, int& sq, int& sk) {
+  bool bad = false;
+  sq = Nq;
+  sk = Nk;
+  if (lq) {
+    const int x = lq[b];
+    sq = x < 1 ? 1 : (x > Nq ? Nq : x);
+    bad |= sq != x;
+  }
+  if (lk) {
+    const int x = lk[b];
+    sk = x < 1 ? 1 : (x > Nk ? Nk : x);
+    bad |= sk != x;
+  }
+  if (causal && sq > sk) {
+    sq = sk;
+    bad = true;
+  }
+  return bad;
+}
 
 // Heads per CTA scheduling group for a (BH x nblk) grid whose causal CTAs
 // cost nblk - blk units of work plus 'overhead' units each (schedule.cu).

@@ -62,13 +62,13 @@ def load(path: str | None = None):
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, vp,
                                c_size_t, vp]
         lib.fa_bwd.restype = c_int
-        lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int, vp, c_size_t,
-                                  vp]
+        lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int, vp, vp, vp,
+                                  c_size_t, vp]
         lib.fa_fwd_kv.restype = c_int
         lib.fa_fwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
         lib.fa_fwd_kv_workspace_bytes.restype = c_size_t
         lib.fa_bwd_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
-                                  vp, c_size_t, vp]
+                                  vp, vp, vp, c_size_t, vp]
         lib.fa_bwd_kv.restype = c_int
         lib.fa_bwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
         lib.fa_bwd_kv_workspace_bytes.restype = c_size_t
@@ -118,9 +118,10 @@ def fa_fwd_kv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
 
 
 def fa_fwd_kv(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: bool,
-              workspace=None, workspace_bytes: int = 0, stream=None) -> int:
+              seqlens_q=None, seqlens_k=None, workspace=None, workspace_bytes: int = 0, stream=None) -> int:
     return int(load().fa_fwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), B, H, Nq, Nk, d, float(scale),
-                                int(bool(causal)), _addr(workspace), int(workspace_bytes), _stream(stream)))
+                                int(bool(causal)), _addr(seqlens_q), _addr(seqlens_k), _addr(workspace),
+                                int(workspace_bytes), _stream(stream)))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -139,14 +140,25 @@ def fa_bwd_kv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
 
 
 def fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: bool,
-              workspace, workspace_bytes: int, stream=None) -> int:
+              seqlens_q, seqlens_k, workspace, workspace_bytes: int, stream=None) -> int:
     return int(load().fa_bwd_kv(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dO), _addr(dq), _addr(dk),
-                                _addr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)), _addr(workspace),
-                                int(workspace_bytes), _stream(stream)))
+                                _addr(dv), B, H, Nq, Nk, d, float(scale), int(bool(causal)), _addr(seqlens_q),
+                                _addr(seqlens_k), _addr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def fa_device_status(reset: bool = True) -> int:
     return int(load().fa_device_status(int(bool(reset))))
+
+
+def _lens(x, B: int):
+    """A per-sequence length tensor as the library takes it: int32, [B], contiguous, on the GPU."""
+    if x is None:
+        return None
+    import torch
+
+    if x.dtype != torch.int32 or tuple(x.shape) != (B,) or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("sequence lengths must be a contiguous int32 CUDA tensor of shape [B]")
+    return x
 
 
 def _shape(q):
@@ -169,9 +181,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     return o, lse
 
 
-def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split: bool = True, stream=None):
+def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split: bool = True, seqlens_q=None,
+               seqlens_k=None, stream=None):
     """Nq query rows against Nk keys: allocate o, lse (and, with ``split``, the key-range
-    workspace fa_fwd_kv_workspace_bytes asks for) with torch and run fa_fwd_kv. Returns (o, lse)."""
+    workspace fa_fwd_kv_workspace_bytes asks for) with torch and run fa_fwd_kv. ``seqlens_q`` /
+    ``seqlens_k`` are optional int32 [B] device tensors (padding masks). Returns (o, lse)."""
     import torch
 
     B, H, Nq, d = _shape(q)
@@ -181,7 +195,8 @@ def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split:
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     need = fa_fwd_kv_workspace_bytes(B, H, Nq, Nk, d) if split else 0
     ws = torch.empty(need, dtype=torch.uint8, device=q.device) if need else None
-    st = fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, ws, need, stream)
+    st = fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, _lens(seqlens_q, B), _lens(seqlens_k, B), ws,
+                   need, stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd_kv")
     return o, lse
@@ -204,8 +219,10 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
-def backward_kv(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, stream=None):
-    """Nq query rows against Nk keys: allocate dq, dk, dv and the workspace with torch and run fa_bwd_kv."""
+def backward_kv(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None, seqlens_q=None,
+                seqlens_k=None, stream=None):
+    """Nq query rows against Nk keys: allocate dq, dk, dv and the workspace with torch and run fa_bwd_kv
+    (``seqlens_q`` / ``seqlens_k`` as in forward_kv)."""
     import torch
 
     B, H, Nq, d = _shape(q)
@@ -214,7 +231,8 @@ def backward_kv(q, k, v, o, lse, dO, causal: bool = False, scale: float | None =
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d)
     ws = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, ws, need, stream)
+    st = fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, _lens(seqlens_q, B),
+                   _lens(seqlens_k, B), ws, need, stream)
     if st != FA_OK:
         raise FAError(st, "fa_bwd_kv")
     return dq, dk, dv

@@ -97,6 +97,19 @@ FA_API size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  *   lse      [out] fp32 [B, H, Nq], lse[i] = ln sum_{j visible to i} exp(scale q_i . k_j)
  *   causal   key j is visible to query i iff j <= i + Nk - Nq; needs Nq <= Nk
  *            (FA_ERR_INVALID_ARG otherwise, since the first rows would see no key)
+ *   seqlens_q, seqlens_k
+ *            [in]  optional device int32 [B] (NULL: every sequence has Nq
+ *            rows / Nk keys), 4-byte aligned: padding masks for a batch of
+ *            sequences of different lengths stored at the full size.
+ *            Sequence b has only its first sq = seqlens_q[b] query rows and
+ *            sk = seqlens_k[b] keys, with the causal rule above written for
+ *            those lengths (j <= i + sk - sq). Rows i >= sq get o = 0 and
+ *            lse = -inf; keys j >= sk are seen by no row. The padding
+ *            entries of q, k, v are never used for a result but must hold
+ *            finite values: the blocks that straddle a length multiply them
+ *            by zero weights. Lengths are read on the device: one outside
+ *            [1, Nq] / [1, Nk] (or, under causal, sq > sk) is clamped into
+ *            range and reported by fa_device_status as FA_ERR_INVALID_ARG.
  *   workspace, workspace_bytes
  *            optional (NULL / 0: one pass over the keys per query block). With
  *            fa_fwd_kv_workspace_bytes bytes (or fewer: then fewer ranges), a
@@ -104,11 +117,12 @@ FA_API size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  *            each range's O / l and logsumexp, and merges them with the
  *            running-maximum rule of chapter 08 written for logsumexps:
  *            lse = m + ln sum_z e^(lse_z - m), o = sum_z e^(lse_z - lse) o_z.
- * fa_fwd(..., N, ...) is fa_fwd_kv(..., N, N, ..., NULL, 0, stream).
+ * fa_fwd(..., N, ...) is fa_fwd_kv(..., N, N, ..., NULL, NULL, NULL, 0, stream).
  * Returns FA_OK or an fa_status error code.
  */
 FA_API int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                     int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+                     int d, float scale, int causal, const int* seqlens_q, const int* seqlens_k, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of device workspace fa_bwd needs for this shape: the fp32 row terms
@@ -142,13 +156,18 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
  * needs Nq <= Nk). q, o, dO, dq are [B, H, Nq, d]; k, v, dk, dv [B, H, Nk, d];
  * lse [B, H, Nq] (the logsumexp fa_fwd_kv returned). The workspace holds D
  * for the Nq rows and the work counters: fa_bwd_kv_workspace_bytes bytes,
- * 256-byte aligned. fa_bwd(..., N, ...) is fa_bwd_kv(..., N, N, ...).
+ * 256-byte aligned. seqlens_q, seqlens_k are the padding masks of fa_fwd_kv
+ * (NULL: none), the same as in the forward call: padding rows get dq = 0,
+ * padding keys dk = dv = 0, and the padding entries of q, k, v, o, dO must
+ * hold finite values. fa_bwd(..., N, ...) is fa_bwd_kv(..., N, N, ..., NULL,
+ * NULL, ...).
  * Returns FA_OK or an fa_status error code.
  */
 FA_API size_t fa_bwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d);
 FA_API int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                      void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                     void* workspace, size_t workspace_bytes, void* stream);
+                     const int* seqlens_q, const int* seqlens_k, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /*
  * Largest scratch, in bytes, that fa_bwd_noalloc holds per device: the
@@ -188,9 +207,10 @@ FA_API const char* fa_status_string(int status);
 
 /*
  * Reads (and, if reset != 0, clears) the device-side error word that kernels
- * set when one of their internal waits exceeds its time limit, on the current
- * device. Synchronises the device. Returns FA_OK, FA_ERR_TIMEOUT, or
- * FA_ERR_LAUNCH if the word cannot be read.
+ * set when one of their internal waits exceeds its time limit, or when a
+ * per-sequence length was out of range, on the current device. Synchronises
+ * the device. Returns FA_OK, FA_ERR_TIMEOUT (a wait gave up), FA_ERR_INVALID_ARG
+ * (only lengths were out of range), or FA_ERR_LAUNCH if the word cannot be read.
  */
 FA_API int fa_device_status(int reset);
 

@@ -82,12 +82,15 @@ def test_fwd_rejects_bad_args(lib, args, status):
     (dict(d=32), fa.FA_ERR_UNSUPPORTED),
     (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(ws=A + 8, ws_bytes=4096), fa.FA_ERR_MISALIGNED),
+    (dict(sq=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(sk=A + 1), fa.FA_ERR_MISALIGNED),
 ])
 def test_fwd_kv_rejects_bad_args(lib, args, status):
-    kw = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Nq=8, Nk=64, d=128, scale=0.1, causal=0, ws=None, ws_bytes=0)
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Nq=8, Nk=64, d=128, scale=0.1, causal=0, sq=None, sk=None, ws=None,
+              ws_bytes=0)
     kw.update(args)
     st = fa.fa_fwd_kv(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["B"], kw["H"], kw["Nq"], kw["Nk"], kw["d"],
-                      kw["scale"], kw["causal"], kw["ws"], kw["ws_bytes"], stream=0)
+                      kw["scale"], kw["causal"], kw["sq"], kw["sk"], kw["ws"], kw["ws_bytes"], stream=0)
     assert st == status
 
 
@@ -124,14 +127,16 @@ def test_bwd_rejects_bad_args(lib, args, status):
     (dict(d=80), fa.FA_ERR_UNSUPPORTED),
     (dict(dv=A + 4), fa.FA_ERR_MISALIGNED),
     (dict(ws_bytes=16), fa.FA_ERR_WORKSPACE),
+    (dict(sq=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(sk=A + 3), fa.FA_ERR_MISALIGNED),
 ])
 def test_bwd_kv_rejects_bad_args(lib, args, status):
     kw = dict(q=A, k=A, v=A, o=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=1, Nq=16, Nk=64, d=64, scale=0.125, causal=1,
-              ws=A, ws_bytes=1 << 20)
+              sq=None, sk=None, ws=A, ws_bytes=1 << 20)
     kw.update(args)
     st = fa.fa_bwd_kv(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["dO"], kw["dq"], kw["dk"], kw["dv"], kw["B"],
-                      kw["H"], kw["Nq"], kw["Nk"], kw["d"], kw["scale"], kw["causal"], kw["ws"], kw["ws_bytes"],
-                      stream=0)
+                      kw["H"], kw["Nq"], kw["Nk"], kw["d"], kw["scale"], kw["causal"], kw["sq"], kw["sk"], kw["ws"],
+                      kw["ws_bytes"], stream=0)
     assert st == status
 
 

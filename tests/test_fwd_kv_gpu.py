@@ -81,7 +81,7 @@ def test_small_workspace_uses_fewer_ranges():
     ws = torch.empty(need // 3, dtype=torch.uint8, device="cuda")
     o = torch.empty_like(g["q"])
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
-    st = fa.fa_fwd_kv(g["q"], g["k"], g["v"], o, lse, B, H, Nq, Nk, d, 0.09, True, ws, ws.numel())
+    st = fa.fa_fwd_kv(g["q"], g["k"], g["v"], o, lse, B, H, Nq, Nk, d, 0.09, True, None, None, ws, ws.numel())
     assert st == fa.FA_OK
     parity.check_status()
     check(x, o, lse, 0.09, True)
