@@ -291,3 +291,120 @@ int oracle_max_threads(int nthreads) {
   return 1;
 #endif
 }
+
+/*
+ * 8-bit forward (the FP8 mode of the third version: "FlashAttention does more
+ * arithmetic to move less data", the section on the later versions, and
+ * "FlashAttention and GPU Memory", chapter 11). The pages say only that the
+ * inputs are 8-bit floats and that rounding to them loses precision; the
+ * readings taken here:
+ *
+ *   - q, k, v arrive as E4M3 codes (the OCP 8-bit float: 1 sign bit, 4
+ *     exponent bits with bias 7, 3 mantissa bits, subnormals, no infinities,
+ *     S.1111.111 = NaN, largest finite 448) with one dequantisation factor per
+ *     tensor: q = desc_q * e4m3(q8), and so on;
+ *   - the scores, the row maximum and the row sum of exponentials are exact
+ *     functions of those values (lse is the exact logsumexp);
+ *   - the probabilities feed the second product as E4M3 too (both operands of
+ *     an 8-bit product are 8-bit). They are rounded at a per-row power-of-two
+ *     scale: with x_ij = s_ij log2(e) and X_i = ceil(max_j x_ij),
+ *       w_ij = 2^(x_ij - X_i + 6)          (in (0, 64], so never saturated)
+ *       p_ij = rn_e4m3(w_ij)               (round to nearest, ties to even)
+ *       o_i  = sum_j p_ij v_j / sum_j w_ij
+ *     Because the scale is a power of two, rounding at any other integer
+ *     reference gives the same p_ij up to that power of two (away from the
+ *     subnormal range), so the result does not depend on the order in which
+ *     the keys are visited. With round_p = 0, p_ij = w_ij and o_i is exact.
+ */
+#define E4M3_MAX 448.0
+
+/* Value of an E4M3 code. */
+double oracle_e4m3_decode(int code) {
+  const int b = code & 0xFF;
+  const int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)m / 8.0, -6); /* subnormal: m/8 * 2^(1 - 7) */
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* x rounded to the nearest E4M3 value (ties to even), saturated at +-448. */
+double oracle_e4m3_round(double x) {
+  if (isnan(x)) return NAN;
+  const double a = fabs(x);
+  double r;
+  if (a >= E4M3_MAX) {
+    r = E4M3_MAX;
+  } else if (a < ldexp(1.0, -6)) {
+    r = ldexp(nearbyint(ldexp(a, 9)), -9); /* subnormal spacing 2^-9 */
+  } else {
+    int ex;
+    frexp(a, &ex); /* a = f 2^ex, f in [0.5, 1): leading bit 2^(ex - 1) */
+    const int q = ex - 1 - 3; /* three mantissa bits: spacing 2^(ex - 4) */
+    r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r > E4M3_MAX) r = E4M3_MAX;
+  }
+  return x < 0 ? -r : r;
+}
+
+int oracle_fwd_fp8(const unsigned char* q8, const unsigned char* k8, const unsigned char* v8, double desc_q,
+                   double desc_k, double desc_v, double* o, double* lse, int BH, int N, int d, double scale,
+                   int causal, int round_p, const int* rows, int nrows, int nthreads) {
+  if (BH < 1 || N < 1 || d < 1 || !q8 || !k8 || !v8 || !o || !lse) return -1;
+  if (!rows) nrows = N;
+  for (int r = 0; rows && r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return -1;
+  set_threads(nthreads);
+  const double log2e = 1.4426950408889634074;
+  int failed = 0;
+  const long long total = (long long)BH * nrows;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* qi = (double*)malloc(sizeof(double) * (size_t)d);
+    double* kj = (double*)malloc(sizeof(double) * (size_t)d);
+    if (!s || !qi || !kj) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long long w = 0; w < total; ++w) {
+      if (!s || !qi || !kj) continue;
+      const int h = (int)(w / nrows);
+      const int i = rows ? rows[w % nrows] : (int)(w % nrows);
+      const unsigned char* qrow = q8 + ((size_t)h * N + i) * d;
+      for (int t = 0; t < d; ++t) qi[t] = desc_q * oracle_e4m3_decode(qrow[t]);
+      const int n = causal ? i + 1 : N;
+      double M = -INFINITY;
+      for (int j = 0; j < n; ++j) {
+        const unsigned char* krow = k8 + ((size_t)h * N + j) * d;
+        for (int t = 0; t < d; ++t) kj[t] = desc_k * oracle_e4m3_decode(krow[t]);
+        s[j] = scale * dot(qi, kj, d);
+        if (s[j] > M) M = s[j];
+      }
+      double l = 0.0; /* exact logsumexp */
+      for (int j = 0; j < n; ++j) l += exp(s[j] - M);
+      lse[(size_t)h * N + i] = M + log(l);
+      const double X = ceil(M * log2e);
+      double wsum = 0.0;
+      double* oi = o + ((size_t)h * N + i) * d;
+      for (int t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int j = 0; j < n; ++j) {
+        const double wj = exp2(s[j] * log2e - X + 6.0);
+        const double pj = round_p ? oracle_e4m3_round(wj) : wj;
+        wsum += wj;
+        const unsigned char* vrow = v8 + ((size_t)h * N + j) * d;
+        for (int t = 0; t < d; ++t) oi[t] += pj * desc_v * oracle_e4m3_decode(vrow[t]);
+      }
+      for (int t = 0; t < d; ++t) oi[t] /= wsum;
+    }
+    free(s);
+    free(qi);
+    free(kj);
+  }
+  return failed ? -1 : 0;
+}

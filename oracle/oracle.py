@@ -23,7 +23,8 @@ Arrays are numpy float64 of shape [BH, N, d] (lse and D: [BH, N]). The
 [BH, Nk, d]); causal then lets row i see keys 0 .. i + Nk - Nq, so the last
 row sees every key as in a decoding step, and ``merge_partials`` combines the
 results of disjoint key ranges with the logsumexp form of the chapter-08
-update rule.
+update rule. ``fwd_fp8`` is the 8-bit forward (E4M3 inputs with one scale
+per tensor, probabilities rounded to E4M3 for the second product).
 """
 from __future__ import annotations
 
@@ -75,6 +76,14 @@ def load(path: str | None = None):
         lib.oracle_bwd_kv.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_double, c_int,
                                       ip, ip, ip, c_int, ip, c_int, c_int]
         lib.oracle_bwd_kv.restype = c_int
+        u8p = ctypes.POINTER(ctypes.c_ubyte)
+        lib.oracle_e4m3_decode.argtypes = [c_int]
+        lib.oracle_e4m3_decode.restype = c_double
+        lib.oracle_e4m3_round.argtypes = [c_double]
+        lib.oracle_e4m3_round.restype = c_double
+        lib.oracle_fwd_fp8.argtypes = [u8p, u8p, u8p, c_double, c_double, c_double, dp, dp, c_int, c_int, c_int,
+                                       c_double, c_int, c_int, ip, c_int, c_int]
+        lib.oracle_fwd_fp8.restype = c_int
         lib.oracle_max_threads.argtypes = [c_int]
         lib.oracle_max_threads.restype = c_int
         if path is None:
@@ -217,6 +226,51 @@ def bwd_kv(q, k, v, dO, scale: float, causal: bool, qrows=None, keys=None, nthre
 # --------------------------------------------------------------------------
 # The standard, materialised computation (tiny inputs only).
 # --------------------------------------------------------------------------
+def e4m3_decode(code: int, lib=None) -> float:
+    """Value of one E4M3 code (0..255)."""
+    return float((lib or load()).oracle_e4m3_decode(int(code)))
+
+
+def e4m3_round(x: float, lib=None) -> float:
+    """x rounded to the nearest E4M3 value (ties to even), saturated at +-448."""
+    return float((lib or load()).oracle_e4m3_round(float(x)))
+
+
+def _u8(a) -> np.ndarray:
+    """Contiguous uint8 codes of a numpy array or a (CPU) torch tensor of E4M3 codes or float8 values."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").contiguous().view(dtype=__import__("torch").uint8).numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise ValueError("expected uint8 E4M3 codes")
+    return a.reshape(-1, a.shape[-2], a.shape[-1])
+
+
+def fwd_fp8(q8, k8, v8, desc_q: float, desc_k: float, desc_v: float, scale: float, causal: bool, round_p=True,
+            rows=None, nthreads: int = 0, lib=None):
+    """8-bit forward: q, k, v are E4M3 codes [BH, N, d] with one dequantisation factor per tensor.
+
+    lse is the exact logsumexp of the scores of the dequantised inputs; o uses the
+    probabilities rounded to E4M3 at the per-row power-of-two scale 2^(6 - ceil(max_j x_ij)),
+    x = scores * log2(e), and divides by the unrounded sum (``round_p=False``: exact
+    attention on the dequantised inputs). ``rows`` as in ``fwd``.
+    """
+    lib = lib or load()
+    q3, k3, v3 = _u8(q8), _u8(k8), _u8(v8)
+    BH, N, d = q3.shape
+    o = np.full((BH, N, d), np.nan)
+    lse = np.full((BH, N), np.nan)
+    ridx, nr = _iptr(rows)
+    u8p = ctypes.POINTER(ctypes.c_ubyte)
+    rc = lib.oracle_fwd_fp8(q3.ctypes.data_as(u8p), k3.ctypes.data_as(u8p), v3.ctypes.data_as(u8p), float(desc_q),
+                            float(desc_k), float(desc_v), _dptr(o), _dptr(lse), BH, N, d, float(scale), int(causal),
+                            int(bool(round_p)),
+                            None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nr, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_fwd_fp8 failed")
+    return o, lse
+
+
 def _mask(N: int, causal: bool) -> np.ndarray:
     """True where key j is visible to query i: every j, or j <= i when causal."""
     allowed = np.ones((N, N), dtype=bool)

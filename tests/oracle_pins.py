@@ -359,6 +359,87 @@ def pin_padding_lengths_are_truncation(lib=None):
         raise AssertionError("causal with more query rows than keys in a head must be refused")
 
 
+def _fp8_codes(seed, BH, N, d):
+    """E4M3 codes of N(0, 1) draws scaled so that the largest lands on 448, and the dequantisation factor."""
+    x = torch.from_numpy(np.random.default_rng(seed).standard_normal((BH, N, d)))
+    desc = float(x.abs().max()) / 448.0
+    return (x / desc).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy(), desc
+
+
+def _e4m3_values(codes):
+    """Values of E4M3 codes by torch's float8_e4m3fn type (the library routine)."""
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_matches_torch(lib=None):
+    """The oracle's E4M3 decoding of all 256 codes and its rounding (ties to even, subnormals) equal
+    torch's float8_e4m3fn type; values beyond 448 saturate (the saturating conversion)."""
+    lib = lib or orc.load()
+    ref = _e4m3_values(np.arange(256, dtype=np.uint8))
+    mine = np.array([orc.e4m3_decode(c, lib=lib) for c in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(mine))
+    assert np.array_equal(ref[~np.isnan(ref)], mine[~np.isnan(mine)])
+    pos = np.unique(ref[(ref >= 0) & ~np.isnan(ref)])
+    mids = (pos[:-1] + pos[1:]) / 2  # exact ties: ties go to the even code
+    rng = np.random.default_rng(5)
+    x = np.concatenate([pos, mids, -mids, *(rng.standard_normal(4000) * sc for sc in (3e-3, 0.05, 1.0, 30.0))])
+    x = x[np.abs(x) < 448]
+    want = torch.from_numpy(x).float().to(torch.float8_e4m3fn).double().numpy()
+    got = np.array([orc.e4m3_round(v, lib=lib) for v in x])
+    assert np.array_equal(want, got), x[want != got][:5]
+    assert orc.e4m3_round(1000.0, lib=lib) == 448.0 and orc.e4m3_round(-460.0, lib=lib) == -448.0
+
+
+def pin_fp8_unrounded_is_exact_attention(lib=None):
+    """Without the rounding of P, the 8-bit forward is exact attention on the dequantised inputs (the
+    pinned fp64 oracle); lse is that attention's logsumexp with or without the rounding."""
+    BH, N, d = 2, 23, 16
+    (q8, dq), (k8, dk), (v8, dv) = (_fp8_codes(s, BH, N, d) for s in (180, 181, 182))
+    q, k, v = _e4m3_values(q8) * dq, _e4m3_values(k8) * dk, _e4m3_values(v8) * dv
+    for causal in (False, True):
+        o_ref, lse_ref = orc.fwd(q, k, v, 0.3, causal)
+        o, lse = orc.fwd_fp8(q8, k8, v8, dq, dk, dv, 0.3, causal, round_p=False, lib=lib)
+        assert np.allclose(o, o_ref, rtol=0, atol=1e-12) and np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+        o_r, lse_r = orc.fwd_fp8(q8, k8, v8, dq, dk, dv, 0.3, causal, lib=lib)
+        assert np.allclose(lse_r, lse_ref, rtol=0, atol=1e-12)
+        err = np.abs(o_r - o_ref).max()
+        assert 1e-6 < err < 0.1 * np.abs(o_ref).max(), err  # the rounding of P is applied, and is small
+
+
+def pin_fp8_zero_q(lib=None):
+    """Q = 0: every scaled exponential is 2^6, which E4M3 holds exactly, so o is the mean of the visible
+    values (prefix means under the causal mask) and lse = ln of the number of visible keys."""
+    BH, N, d = 2, 19, 8
+    (v8, dv), (k8, dk) = _fp8_codes(190, BH, N, d), _fp8_codes(191, BH, N, d)
+    q8 = np.zeros((BH, N, d), dtype=np.uint8)
+    v = _e4m3_values(v8) * dv
+    o, lse = orc.fwd_fp8(q8, k8, v8, 1.0, dk, dv, 0.7, False, lib=lib)
+    assert np.allclose(o, v.mean(axis=1, keepdims=True), rtol=0, atol=1e-13)
+    assert np.allclose(lse, math.log(N), rtol=0, atol=1e-13)
+    o, lse = orc.fwd_fp8(q8, k8, v8, 1.0, dk, dv, 0.7, True, lib=lib)
+    prefix = np.cumsum(v, axis=1) / np.arange(1, N + 1)[None, :, None]
+    assert np.allclose(o, prefix, rtol=0, atol=1e-13)
+    assert np.allclose(lse, np.log(np.arange(1, N + 1))[None, :], rtol=0, atol=1e-13)
+
+
+def pin_fp8_rounding_brute_force(lib=None):
+    """The rounded-P forward on a tiny case, written with numpy and torch's float8_e4m3fn rounding:
+    p = e4m3(2^(x - ceil(max x) + 6)), o = sum p v / sum 2^(x - ceil(max x) + 6)."""
+    BH, N, d = 2, 6, 4
+    (q8, dq), (k8, dk), (v8, dv) = (_fp8_codes(s, BH, N, d) for s in (200, 201, 202))
+    q, k, v = _e4m3_values(q8) * dq, _e4m3_values(k8) * dk, _e4m3_values(v8) * dv
+    scale = 0.9
+    for causal in (False, True):
+        o, _ = orc.fwd_fp8(q8, k8, v8, dq, dk, dv, scale, causal, lib=lib)
+        for h in range(BH):
+            for i in range(N):
+                n = i + 1 if causal else N
+                x = np.array([scale * float(q[h, i] @ k[h, j]) for j in range(n)]) / math.log(2)
+                w = np.exp2(x - math.ceil(x.max()) + 6)
+                p = torch.from_numpy(w).to(torch.float8_e4m3fn).double().numpy()
+                assert np.allclose(o[h, i], (p[:, None] * v[h, :n]).sum(axis=0) / w.sum(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_zero_q_noncausal,
     pin_zero_q_causal,
@@ -380,4 +461,8 @@ ALL_PINS = [
     pin_kv_bwd_torch_autograd,
     pin_kv_bwd_suffix_of_self_attention,
     pin_padding_lengths_are_truncation,
+    pin_e4m3_matches_torch,
+    pin_fp8_unrounded_is_exact_attention,
+    pin_fp8_zero_q,
+    pin_fp8_rounding_brute_force,
 ]

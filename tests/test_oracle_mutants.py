@@ -32,6 +32,12 @@ MUTANTS = [
      "for (int i = causal && j >= off ? j - off + 1 : 0; i < a; ++i)"),
     ("bwd_mask_reversed", "for (int i = causal && j > off ? j - off : 0; i < a; ++i)",
      "for (int i = 0; i < (causal ? (j - off + 1 > 0 ? j - off + 1 : 0) : a) && i < a; ++i)"),
+    ("e4m3_exponent_bias_8", "v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_round_truncates", "r = ldexp(nearbyint(ldexp(a, -q)), q);", "r = ldexp(floor(ldexp(a, -q)), q);"),
+    ("fp8_sum_of_rounded_p", "wsum += wj;", "wsum += pj;"),
+    ("fp8_dropped_v_scale", "oi[t] += pj * desc_v * oracle_e4m3_decode(vrow[t]);",
+     "oi[t] += pj * oracle_e4m3_decode(vrow[t]);"),
+    ("fp8_causal_skips_diagonal", "const int n = causal ? i + 1 : N;", "const int n = causal ? i : N;"),
     ("dp_uses_o_index", "dp[j] = dot(dOi, v + kb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + kb + (size_t)i * d, d);"),
 ]
 
