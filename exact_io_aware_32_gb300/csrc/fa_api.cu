@@ -145,6 +145,7 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.Nk = Nk;
   a.d = d;
   a.scale_log2 = (float)((double)scale * kLog2e);
+  a.o_scale = 1.0f;
   a.causal = causal ? 1 : 0;
   a.seqlens_q = seqlens_q;
   a.seqlens_k = seqlens_k;
@@ -163,6 +164,46 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.o_part = static_cast<float*>(workspace);
     a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * d * sizeof(float)));
   }
+  return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k, float descale_v,
+               void* o, float* lse, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const float desc[3] = {descale_q, descale_k, descale_v};
+  for (float x : desc)
+    if (!(x > 0.0f) || !std::isfinite(x)) return FA_ERR_INVALID_ARG;
+  const float scale_log2 = (float)((double)scale * (double)descale_q * (double)descale_k * kLog2e);
+  if (!std::isfinite(scale_log2) || !(scale_log2 > 0.0f)) return FA_ERR_INVALID_ARG;  // over- or underflow
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const int BH = B * H;
+  // E4M3 rows of 128 bytes: one 128 x 128-byte box per tile
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BH, N, d, 128, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BH, N, d, 128, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BH, N, d, 128, 128) ||
+      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.status = di->status;
+  a.BH = BH;
+  a.H = H;
+  a.Nq = N;
+  a.Nk = N;
+  a.d = d;
+  a.scale_log2 = scale_log2;
+  a.o_scale = descale_v;
+  a.fp8 = 1;
+  a.causal = causal ? 1 : 0;
+  a.split_blocks = (N + 127) / 128;
+  a.n_split = 1;
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

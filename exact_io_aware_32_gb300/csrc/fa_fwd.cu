@@ -34,26 +34,38 @@ using namespace fa::ptx;
 
 constexpr float kLn2 = 0.693147180559945309417f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// 8-bit P: the reference is an integer and P = 2^(x - m_ref + kP8Bias) with
+// x <= m_ref + kP8Lag, so P <= 2^8 (E4M3 holds up to 448) and rounding P at
+// any reference gives the same values up to a power of two.
+constexpr float kP8Bias = 6.0f;
+constexpr float kP8Lag = 2.0f;
 
-template <int D>
+// FP8: q, k, v are E4M3 (one byte per element) and both products use 8-bit
+// operands (P is rounded to E4M3); o stays bf16.
+template <int D, bool FP8 = false>
 struct FwdCfg {
   static constexpr int BM = 128;                 // query rows per tile = TMEM lanes
   static constexpr int BN = 128;                 // keys per block
-  static constexpr int kPanels = D / 64;         // 128-byte-wide column panels per row
+  static constexpr int kElem = FP8 ? 1 : 2;      // bytes per input element
+  static constexpr int kPanels = D * kElem / 128;  // 128-byte-wide column panels per input row
   static constexpr int kPanelBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int kTileBytes = kPanels * kPanelBytes;
+  static constexpr int kOPanels = D / 64;        // panels of a bf16 output row
+  // a query tile's slot also stages that tile's bf16 O for the store
+  static constexpr int kQSlotBytes = (kPanels > kOPanels ? kPanels : kOPanels) * kPanelBytes;
+  static constexpr int kKStep = FP8 ? 32 : 16;   // K of one MMA instruction
   // K of a block is released once both tiles' S have read it, V only once both
   // PV products have: V gets the deeper ring, so its load has more than one
   // block's time to land.
-  static constexpr int kKStages = D == 128 ? 2 : 4;
-  static constexpr int kVStages = D == 128 ? 3 : 4;
+  static constexpr int kKStages = FP8 ? 4 : (D == 128 ? 2 : 4);
+  static constexpr int kVStages = FP8 ? 4 : (D == 128 ? 3 : 4);
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffK = kOffQ + 2 * kQSlotBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-  // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 reuses its first 64)
-  // and O_t (fp32, D columns) for query tiles t = 0, 1.
+  // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 reuses its first 64,
+  // as E4M3 its first 32) and O_t (fp32, D columns) for query tiles t = 0, 1.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128u; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
   static constexpr int kThreads = 320;
@@ -80,9 +92,10 @@ __device__ inline void zero_rows(const FwdArgs& a, int bh, int r0, int n, int ti
 
 // VARLEN: per-sequence lengths are given (padding masks); without them the
 // lengths are the array sizes, which the kernel then takes as constants.
-template <int D, bool CAUSAL, bool VARLEN>
+// FP8: E4M3 inputs and 8-bit products (FwdCfg).
+template <int D, bool CAUSAL, bool VARLEN, bool FP8 = false>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FwdBarriers& bars = *reinterpret_cast<FwdBarriers*>(smem + C::kOffBar);
@@ -165,7 +178,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars.q_full[t], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full[t], pn * 64,
+          tma_load_3d(smem + C::kOffQ + t * C::kQSlotBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full[t],
+                      pn * (128 / C::kElem),
                       qblk * 256 + t * 128, bh);
       }
       __syncwarp();
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(&bars.k_full[sk], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffK + sk * C::kTileBytes + pn * C::kPanelBytes, &a.tm_k, &bars.k_full[sk],
-                      pn * 64, (jb + j) * C::BN, bh);
+                      pn * (128 / C::kElem), (jb + j) * C::BN, bh);
       }
       __syncwarp();
       nk_issued = j + 1;
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mbar_arrive_expect_tx(&bars.v_full[sv], C::kTileBytes);
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffV + sv * C::kTileBytes + pn * C::kPanelBytes, &a.tm_v, &bars.v_full[sv],
-                      pn * 64, (jb + j) * C::BN, bh);
+                      pn * (128 / C::kElem), (jb + j) * C::BN, bh);
       }
       __syncwarp();
       nv_issued = j + 1;
@@ -218,8 +232,9 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // ops (elect.sync picks the lowest active lane, so always the same one,
     // which matters because a commit tracks the issuing thread's MMAs).
     {
-      constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);  // Q, K both K-major
-      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);       // P from TMEM, V MN-major
+      // Q, K both K-major; P from TMEM, V MN-major
+      constexpr uint32_t kIdS = FP8 ? idesc_e4m3(128, C::BN, false, false) : idesc_bf16(128, C::BN, false, false);
+      constexpr uint32_t kIdO = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       const uint32_t k_base = smem_u32(smem + C::kOffK);
       const uint32_t v_base = smem_u32(smem + C::kOffV);
@@ -229,11 +244,14 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const uint64_t dv0 = sdesc_sw128(v_base, C::kPanelBytes, 1024);
       auto issue_s = [&](int t, int st) {  // by the elected lane
         const uint32_t d_s = tmem + C::col_s(t);
-        const uint32_t qo = (uint32_t)(t * C::kTileBytes) >> 4, ko = (uint32_t)(st * C::kTileBytes) >> 4;
+        const uint32_t qo = (uint32_t)(t * C::kQSlotBytes) >> 4, ko = (uint32_t)(st * C::kTileBytes) >> 4;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / C::kKStep; ++kk) {  // each k-step reads 32 bytes of every row
           const uint32_t off = ((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4;
-          mma_ss(d_s, dq0 + qo + off, dk0 + ko + off, kIdS, kk > 0);
+          if constexpr (FP8)
+            mma_ss_f8(d_s, dq0 + qo + off, dk0 + ko + off, kIdS, kk > 0);
+          else
+            mma_ss(d_s, dq0 + qo + off, dk0 + ko + off, kIdS, kk > 0);
         }
         mma_commit(&bars.s_full[t]);
       };
@@ -277,9 +295,16 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
               const uint32_t a_p = tmem + C::col_s(t);
               const uint32_t d_o = tmem + C::col_o(t);
               const uint32_t vo = (uint32_t)(s * C::kTileBytes) >> 4;
+              // k-step kk: P columns [8 kk, 8 kk + 8) (32 bytes of each row), V rows [kk kKStep, +kKStep)
 #pragma unroll
-              for (int kk = 0; kk < C::BN / 16; ++kk)
-                mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * (2048 >> 4), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < C::BN / C::kKStep; ++kk) {
+                if constexpr (FP8)
+                  mma_ts_f8(d_o, a_p + kk * 8, dv0 + vo + kk * ((C::kKStep * 128) >> 4), kIdO,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+                else
+                  mma_ts(d_o, a_p + kk * 8, dv0 + vo + kk * ((C::kKStep * 128) >> 4), kIdO,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+              }
               // only the epilogue waits for O (the softmax learns of earlier PV products through
               // the S products issued after them), so only the last one is committed
               if (j == nb[t] - 1) mma_commit(&bars.o_done[t]);
@@ -346,31 +371,65 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         mx1 = fmax3(mx1, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]));
       }
       const float mx = fmaxf(mx0, mx1);
-      const float m_new = fmaxf(m_ref, mx * sl2);
       float alpha = 1.f;
-      const bool move = m_new > m_ref + kRescaleThreshold;
-      if (move) {
-        alpha = ex2(m_ref - m_new);
-        m_ref = m_new;
+      bool move;
+      if constexpr (FP8) {
+        // integer reference, moved to ceil(max) once the max passes it by more than kP8Lag
+        const float xm = mx * sl2;
+        move = xm > m_ref + kP8Lag;
+        if (move) {
+          const float m_new = ceilf(xm);
+          alpha = exp2_int_nonpos(m_ref - m_new);  // exact, so earlier rounded P stay exact multiples
+          m_ref = m_new;
+        }
+      } else {
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        move = m_new > m_ref + kRescaleThreshold;
+        if (move) {
+          alpha = ex2(m_ref - m_new);
+          m_ref = m_new;
+        }
       }
       const bool rescale = __any_sync(0xffffffffu, move && j > 0);
       float2 sum = make_float2(0.f, 0.f);
       // a row that has seen no key yet (possible within a key range) keeps m_ref = -inf and P = 0
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      const float m_use = (m_ref == -INFINITY ? 0.f : m_ref) - (FP8 ? kP8Bias : 0.f);
       const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_use, -m_use);
-      // P as bf16 pairs over the first 64 columns of S_t (all of S_t is already in
-      // registers), 32 scores at a time.
+      if constexpr (FP8) {
+        // P as E4M3, four per column, over the first 32 columns of S_t; the row sum
+        // takes P before rounding (the sum of the exponentials, as in the 16-bit path)
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), scale2, shift2);
-          const float2 p = make_float2(ex2(x.x), ex2(x.y));
-          sum = fadd2(sum, p);
-          pk[c >> 1] = pack_bf16x2(p.x, p.y);
+          for (int c = 0; c < 64; c += 4) {
+            const int ch = 2 * half + (c >> 5), cc = c & 31;
+            const float2 x0 =
+                ffma2(make_float2(__uint_as_float(sr[ch][cc]), __uint_as_float(sr[ch][cc + 1])), scale2, shift2);
+            const float2 x1 =
+                ffma2(make_float2(__uint_as_float(sr[ch][cc + 2]), __uint_as_float(sr[ch][cc + 3])), scale2, shift2);
+            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
+            sum = fadd2(sum, fadd2(p0, p1));
+            pk[c >> 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+          }
+          tmem_st16(t_s + 16 * half, pk);
         }
-        tmem_st16(t_s + 16 * ch, pk);
+      } else {
+        // P as bf16 pairs over the first 64 columns of S_t (all of S_t is already in
+        // registers), 32 scores at a time.
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x =
+                ffma2(make_float2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), scale2, shift2);
+            const float2 p = make_float2(ex2(x.x), ex2(x.y));
+            sum = fadd2(sum, p);
+            pk[c >> 1] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st16(t_s + 16 * ch, pk);
+        }
       }
       l_sum = l_sum * alpha + (sum.x + sum.y);
       if (rescale) {
@@ -396,7 +455,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       const size_t prow = ((size_t)blockIdx.z * a.BH + bh) * Nq + row;
       if (ok && nbt > 0) {
         tc_fence_after();
-        const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        const float inv_l = l_sum > 0.f ? a.o_scale / l_sum : 0.f;
         float4* orow = reinterpret_cast<float4*>(a.o_part + prow * D);
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
@@ -412,15 +471,15 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         }
       }
       if (ok && row < Nq)
-        a.lse_part[prow] = nbt > 0 && l_sum > 0.f && (!VARLEN || row < sq) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+        a.lse_part[prow] = nbt > 0 && l_sum > 0.f && (!VARLEN || row < sq) ? (m_ref - (FP8 ? kP8Bias : 0.f) + log2f(l_sum)) * kLn2 : -INFINITY;
     } else if (nbt == 0) {
       // every row of this tile is padding (another tile of the CTA is not)
       if (VARLEN && ok) zero_rows<D>(a, bh, r0, min(128, Nq - r0), r, 128);
     } else {  // nbt is uniform over the warpgroup, so every thread reaches the named barrier  // nbt is uniform over the warpgroup, so every thread reaches the named barrier
-      uint8_t* stage = smem + C::kOffQ + t * C::kTileBytes;  // Q_t is no longer read by any MMA
+      uint8_t* stage = smem + C::kOffQ + t * C::kQSlotBytes;  // Q_t is no longer read by any MMA
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.f / l_sum;
+        const float inv_l = a.o_scale / l_sum;
         const bool pad = VARLEN && row >= sq;  // a padding row among valid ones: o = 0
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
@@ -443,13 +502,14 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       named_bar_sync(1 + t, 128);
       if (r == 0 && !*abort_flag) {
-        for (int pn = 0; pn < C::kPanels; ++pn)
+        for (int pn = 0; pn < C::kOPanels; ++pn)
           tma_store_3d(&a.tm_o, stage + pn * C::kPanelBytes, pn * 64, qblk * 256 + t * 128, bh);
         bulk_commit();
         bulk_wait_read0();  // the staging tile has been read; the writes finish on their own
       }
       if (ok && row < Nq)
-        a.lse[(size_t)bh * Nq + row] = !VARLEN || row < sq ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+        a.lse[(size_t)bh * Nq + row] =
+            !VARLEN || row < sq ? (m_ref - (FP8 ? kP8Bias : 0.f) + log2f(l_sum)) * kLn2 : -INFINITY;
     }
   }
 
@@ -499,12 +559,18 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const __grid_constant
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
-  using C = FwdCfg<D>;
   auto kern = a.seqlens_q || a.seqlens_k ? fa_fwd_kernel<D, CAUSAL, true> : fa_fwd_kernel<D, CAUSAL, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  int smem = FwdCfg<D>::kSmemBytes;
+  if constexpr (D == 128) {
+    if (a.fp8) {  // 8-bit inputs: no lengths, no key ranges
+      kern = fa_fwd_kernel<D, CAUSAL, false, true>;
+      smem = FwdCfg<D, true>::kSmemBytes;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + 255) / 256), (unsigned)a.n_split);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  kern<<<grid, 320, smem, stream>>>(a);
   if (a.n_split > 1) {
     const long long rows = (long long)a.BH * a.Nq;
     fa_fwd_merge_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(a);

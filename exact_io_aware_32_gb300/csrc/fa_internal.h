@@ -15,7 +15,9 @@ struct FwdArgs {
   float* lse;              // fp32 [BH][Nq]
   unsigned int* status;    // device error word
   int BH, H, Nq, Nk, d;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (8-bit inputs: times the q and k dequantisation factors)
+  float o_scale;     // factor on O / l: 1, or the v dequantisation factor for 8-bit inputs
+  int fp8;           // q, k, v are E4M3 codes (d = 128 only)
   int causal;        // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
   // optional per-sequence lengths, int32 [B] (padding masks): batch b has only
   // its first seq_len(seqlens_q, b, Nq) query rows and seq_len(seqlens_k, b, Nk) keys

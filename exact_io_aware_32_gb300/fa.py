@@ -2,11 +2,11 @@
 
 Argument marshalling only: every step of attention runs in the CUDA kernels
 of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
-``fa_fwd_kv_workspace_bytes``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
+``fa_fwd_kv_workspace_bytes``, ``fa_fwd_fp8``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
 ``fa_bwd_kv_workspace_bytes``,
 ``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
 torch CUDA tensors or raw device addresses (ints). ``forward``,
-``forward_kv``, ``backward`` and ``backward_kv`` are conveniences that
+``forward_kv``, ``forward_fp8``, ``backward`` and ``backward_kv`` are conveniences that
 allocate the outputs with torch.
 
 If the library has not been built, or cannot be loaded, every call raises:
@@ -29,8 +29,8 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_kv",
-            "fa_bwd_kv_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
+EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
+            "fa_bwd_kv", "fa_bwd_kv_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +65,9 @@ def load(path: str | None = None):
         lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int, vp, vp, vp,
                                   c_size_t, vp]
         lib.fa_fwd_kv.restype = c_int
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, c_float, c_float, c_float, vp, vp, c_int, c_int, c_int, c_int, c_float,
+                                   c_int, vp]
+        lib.fa_fwd_fp8.restype = c_int
         lib.fa_fwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
         lib.fa_fwd_kv_workspace_bytes.restype = c_size_t
         lib.fa_bwd_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
@@ -124,6 +127,12 @@ def fa_fwd_kv(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: 
                                 int(workspace_bytes), _stream(stream)))
 
 
+def fa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, o, lse, B: int, H: int, N: int, d: int,
+               scale: float, causal: bool, stream=None) -> int:
+    return int(load().fa_fwd_fp8(_addr(q), _addr(k), _addr(v), float(descale_q), float(descale_k), float(descale_v),
+                                 _addr(o), _addr(lse), B, H, N, d, float(scale), int(bool(causal)), _stream(stream)))
+
+
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_bytes(B, H, N, d))
 
@@ -178,6 +187,25 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     st = fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
+    return o, lse
+
+
+def forward_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float, causal: bool = False,
+                scale: float | None = None, stream=None):
+    """8-bit forward: q8, k8, v8 are [B, H, N, 128] tensors of E4M3 codes (uint8 or float8_e4m3fn) with
+    per-tensor dequantisation factors; allocate o (bf16) and lse (fp32) and run fa_fwd_fp8. Returns (o, lse)."""
+    import torch
+
+    B, H, N, d = _shape(q8)
+    for x in (q8, k8, v8):
+        if x.element_size() != 1 or not x.is_contiguous():
+            raise ValueError("expected contiguous one-byte E4M3 tensors")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    st = fa_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal, stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return o, lse
 
 

@@ -68,5 +68,25 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_mult: float = 1.0,
     return out
 
 
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int, qk_mult: float = 1.0, device: str = "cpu"):
+    """E4M3 versions of q, k, v for the 8-bit forward: the same float32 draws as
+    make_inputs, each tensor divided by its own factor amax / 448 (so that its
+    largest magnitude lands on the largest E4M3 value) and rounded to E4M3 by
+    torch's float8_e4m3fn conversion. Returns dict(q, k, v) of uint8 code
+    tensors [B, H, N, d] and dict(q, k, v) of the dequantisation factors."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, N, d)
+    x = {name: torch.randn(shape, generator=g, dtype=torch.float32) for name in ("q", "k", "v")}
+    if qk_mult != 1.0:
+        x["q"].mul_(qk_mult)
+        x["k"].mul_(qk_mult)
+    codes, desc = {}, {}
+    for name, t in x.items():
+        desc[name] = float(t.abs().max()) / 448.0
+        codes[name] = (t / desc[name]).to(torch.float8_e4m3fn).view(torch.uint8).to(device)
+    return codes, desc
+
+
 def workload_inputs(w: Workload, device: str = "cpu"):
     return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.qk_mult, device=device)

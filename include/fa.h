@@ -125,6 +125,30 @@ FA_API int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float
                      size_t workspace_bytes, void* stream);
 
 /*
+ * 8-bit forward: the FP8 mode the pages give the third version ("FlashAttention
+ * does more arithmetic to move less data", the section on the later versions;
+ * "FlashAttention and GPU Memory", chapter 11), with both products on 8-bit
+ * tensor-core operands and fp32 accumulation.
+ *   q, k, v  [in]  E4M3 codes (OCP 8-bit float, one byte per element) [B, H, N, d], d = 128
+ *   descale_q, descale_k, descale_v
+ *            [in]  per-tensor dequantisation factors (finite, > 0): the inputs
+ *            are descale_q * e4m3(q), descale_k * e4m3(k), descale_v * e4m3(v)
+ *   o        [out] bf16 [B, H, N, d]
+ *   lse      [out] fp32 [B, H, N], the logsumexp of the scaled scores of the dequantised inputs
+ *   scale, causal as in fa_fwd.
+ * The probabilities enter the second product as E4M3: each row's P is scaled
+ * by a power of two, 2^(6 - m) for an integer reference m at most 2 below the
+ * row maximum of scores * log2(e) (so P never exceeds 2^8 < 448), rounded to
+ * nearest even, and o divides by the sum of the unrounded values. A power-of-
+ * two scale makes the rounded values independent of the reference, hence of
+ * the order in which the keys are visited (outside the subnormal range).
+ * FA_ERR_UNSUPPORTED for d != 128.
+ * Returns FA_OK or an fa_status error code.
+ */
+FA_API int fa_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k, float descale_v,
+                      void* o, float* lse, int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs for this shape: the fp32 row terms
  * D_i = dO_i . o_i [B, H, N], padded to 256 bytes, then 256 bytes of work
  * counters that the backward kernels use to hand out (head, block) tiles to

@@ -104,6 +104,27 @@ def test_fwd_kv_workspace_bytes_without_gpu_or_bad_shape(lib):
 
 
 @pytest.mark.parametrize("args,status", [
+    (dict(v=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=1e30, dk=1e30), fa.FA_ERR_INVALID_ARG),  # scale * dq * dk * log2(e) overflows fp32
+    (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 4), fa.FA_ERR_MISALIGNED),
+])
+def test_fwd_fp8_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, dq=0.01, dk=0.02, dv=0.03, B=1, H=2, N=256, d=128, scale=0.1, causal=1)
+    kw.update(args)
+    st = fa.fa_fwd_fp8(kw["q"], kw["k"], kw["v"], kw["dq"], kw["dk"], kw["dv"], kw["o"], kw["lse"], kw["B"], kw["H"],
+                       kw["N"], kw["d"], kw["scale"], kw["causal"], stream=0)
+    assert st == status
+
+
+@pytest.mark.parametrize("args,status", [
     (dict(dO=0), fa.FA_ERR_INVALID_ARG),
     (dict(d=32), fa.FA_ERR_UNSUPPORTED),
     (dict(dq=A + 2), fa.FA_ERR_MISALIGNED),
