@@ -18,6 +18,10 @@ same workload.
 decoding forward instead (fa_fwd_kv: Nq query rows against a resident cache of
 Nk keys and values, split over key ranges): a step is one call, and the metric
 is the HBM bandwidth of its algorithmic bytes.
+
+``--workload fp8_<B>_<H>_<N>_<causal|noncausal>`` measures the 8-bit forward
+(fa_fwd_fp8, d = 128, E4M3 q, k, v with per-tensor factors): a step is one
+call, and the metric is its matmul TFLOP/s against the 8-bit dense peak.
 """
 from __future__ import annotations
 
@@ -40,6 +44,7 @@ from exact_io_aware_32_gb300 import inputs, model  # noqa: E402
 
 METRIC = "attention fwd and fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 peak"
 DECODE_METRIC = "decoding attention forward (fa_fwd_kv): GB/s of algorithmic HBM bytes (bf16, 1 GB300)"
+FP8_METRIC = "8-bit attention forward (fa_fwd_fp8, E4M3 inputs): TFLOP/s (1 GB300) and % of dense FP8 peak"
 DEFAULT_WORKLOAD = "d128_n4096_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 L2_BYTES = 129e6
@@ -547,6 +552,143 @@ def run_decode(args, c):
         }), flush=True)
 
 
+# ---------------------------------------------------------------------- 8-bit forward
+def fp8_spec(name: str):
+    """'fp8_<B>_<H>_<N>_<causal|noncausal>' -> dict (d = 128), or None."""
+    if not name.startswith("fp8_"):
+        return None
+    parts = name.split("_")
+    B, H, N = (int(x) for x in parts[1:4])
+    return dict(B=B, H=H, N=N, d=128, causal=parts[4] == "causal")
+
+
+def run_fp8(args, c):
+    import torch
+
+    from exact_io_aware_32_gb300 import fa
+    from oracle import oracle as orc
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
+    scale = 1.0 / math.sqrt(d)
+    # N(0, 1) draws on the device, each tensor scaled by amax / 448 and rounded to E4M3 (torch's conversion)
+    g = torch.Generator(device=dev)
+    g.manual_seed(8000 + rank)
+    codes, desc = [], []
+    for _ in range(3):
+        x = torch.randn((B, H, N, d), generator=g, device=dev)
+        desc.append(float(x.abs().max()) / 448.0)
+        codes.append((x / desc[-1]).to(torch.float8_e4m3fn).view(torch.uint8))
+        del x
+    q8, k8, v8 = codes
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = int(stream.cuda_stream)
+
+    def call(xq=q8, xk=k8, xv=v8, xo=o, xl=lse):
+        st = fa.fa_fwd_fp8(xq, xk, xv, desc[0], desc[1], desc[2], xo, xl, B, H, N, d, scale, causal, sp)
+        if st:
+            raise fa.FAError(st, "fa_fwd_fp8")
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.4)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        dist = tdist
+        dist.init_process_group("nccl", device_id=dev)
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    w1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    st = fa.fa_device_status(True)
+    if st != fa.FA_OK:
+        raise fa.FAError(st, "timed region")
+    call_s = statistics.mean(e0.elapsed_time(e1) / 1e3 for e0, e1 in ev)
+    total_s = reduce_max_over_ranks([w0.elapsed_time(w1) / 1e3], dist, dev)[0] if dist else w0.elapsed_time(w1) / 1e3
+    flops = model.fwd_flops(B, H, N, d, causal)
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # end to end: the codes in and o, lse out every step, one stream
+    hin = [x.to("cpu").pin_memory() for x in (q8, k8, v8)]
+    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize(dev)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip((q8, k8, v8), hin):
+            dst.copy_(src, non_blocking=True)
+        call()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = a0.elapsed_time(a1) / 1e3 / e2e_steps
+    cb = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle's 8-bit forward on whole heads of the same shape, for about cpu_budget seconds
+        threads = orc.max_threads(host_cores())
+        x = [t[:1, :1].to("cpu") for t in (q8, k8, v8)]
+        heads, secs = 0, 0.0
+        while heads < B * H and secs < args.cpu_budget:
+            t0 = time.perf_counter()
+            orc.fwd_fp8(x[0], x[1], x[2], desc[0], desc[1], desc[2], scale, causal, nthreads=threads)
+            secs += time.perf_counter() - t0
+            heads += 1
+        cb = {"value": flops / (B * H) * heads / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+              "sample": f"{heads} of {B * H} heads at full N={N}, d={d}, 8-bit forward, fp64, {secs:.1f} s wall"}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        value = flops * world * args.steps / total_s / 1e12
+        achieved = flops / call_s / 1e12
+        print(json.dumps({
+            "metric": FP8_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 o)", "data": "synthetic",
+            "config": {"workload": args.workload, **c,
+                       "l2": f"q, k, v {3 * B * H * N * d / 1e6:.0f} MB and o {B * H * N * d * 2 / 1e6:.0f} MB "
+                             "per call vs 129 MB L2; no flush"},
+            "pct_of_peak": 100.0 * value / fp8_peak,
+            "roofline": {"kernel": "fa_fwd_kernel<128, causal, fp8>", "bound": "tensor", "achieved": achieved,
+                         "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                         "traffic": kernel_traffic("fa_fwd.cu", args.workload),
+                         "peak_basis": f"2 x {peaks['source']} dense bf16 burst (the nominal fp8 : bf16 ratio "
+                                       "4.5 : 2.25); the kernel is timed alone",
+                         "algorithmic_flops_per_launch": flops},
+            "e2e": {"value": flops / e2e_s / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": sum(x.numel() for x in hin),
+                    "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "steps": e2e_steps,
+                    "schedule": "q, k, v codes in and o, lse out every step, one stream"},
+            "gpu_launches": args.steps, "clocks": clk, "cpu_baseline": cb,
+        }), flush=True)
+
+
 # ---------------------------------------------------------------------- reference arm (the oracle)
 def run_reference(args, w, causal: bool):
     rank, world, _ = dist_env()
@@ -597,6 +739,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    c = fp8_spec(args.workload)
+    if c is not None:
+        if args.impl == "reference":
+            raise SystemExit("the 8-bit workloads have no reference arm")
+        run_fp8(args, c)
+        return
     c = decode_spec(args.workload)
     if c is not None:
         if args.impl == "reference":

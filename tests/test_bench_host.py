@@ -28,6 +28,13 @@ def test_workload_names():
         bench.workload_by_name("nope")
 
 
+def test_decode_and_fp8_workload_names():
+    assert bench.decode_spec("decode_8_32_1_16384_128_causal") == dict(B=8, H=32, Nq=1, Nk=16384, d=128, causal=True)
+    assert bench.fp8_spec("fp8_4_32_4096_causal") == dict(B=4, H=32, N=4096, d=128, causal=True)
+    assert bench.fp8_spec("fp8_1_16_16384_noncausal")["causal"] is False
+    assert bench.fp8_spec("d128_n4096_causal") is None and bench.decode_spec("fp8_4_32_4096_causal") is None
+
+
 def test_aggregate_uses_slowest_rank():
     v, t = bench.aggregate([1.0, 2.0, 1.5], [10.0, 10.0, 10.0])
     assert t == 2.0 and v == 15.0
