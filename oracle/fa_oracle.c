@@ -408,3 +408,192 @@ int oracle_fwd_fp8(const unsigned char* q8, const unsigned char* k8, const unsig
   }
   return failed ? -1 : 0;
 }
+
+/*
+ * Dropout ("FlashAttention and GPU Memory", chapter 07: dropout is one of
+ * the steps fused into the single kernel; chapter 09: the backward keeps only
+ * the random-number generator's state and makes the mask again). The pages
+ * fix neither the generator nor the mask's layout; the readings taken here:
+ *
+ *   - the generator is Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ *     "Parallel random numbers: as easy as 1, 2, 3", SC 2011), a counter-based
+ *     generator: ten rounds of
+ *       (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ *     with M0 = 0xD2511F53, M1 = 0xCD9E8D57 and the key (k0, k1) advanced by
+ *     (0x9E3779B9, 0xBB67AE85) after every round;
+ *   - one call covers a block of 4 queries by 4 keys of one head: counter
+ *     (j / 4, i / 4, bh, offset), key (seed mod 2^32, seed / 2^32); output
+ *     word i mod 4, byte j mod 4 (bits 8 (j mod 4) .. + 7) is the element's
+ *     random byte u;
+ *   - the element is kept iff u >= p256, so the dropout probability is
+ *     p256 / 256 (p256 in 0 .. 255), and kept elements are scaled by
+ *     256 / (256 - p256);
+ *   - dropout applies to P after the softmax: lse, m and l are those of the
+ *     undropped scores, and o_i = sum_j P_ij Z_ij v_j with Z_ij = keep / (1 - p).
+ * The backward, by the chain rule with the mask fixed:
+ *   dv_j  = sum_i P_ij Z_ij dO_i
+ *   dP_ij = Z_ij (dO_i . v_j)
+ *   D_i   = sum_j P_ij dP_ij            (= dO_i . o_i)
+ *   dS_ij = P_ij (dP_ij - D_i), dq and dk as without dropout.
+ */
+void oracle_philox4x32_10(const unsigned int ctr[4], const unsigned int key[2], unsigned int out[4]) {
+  unsigned int c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3], k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long p0 = 0xD2511F53ull * c0, p1 = 0xCD9E8D57ull * c2;
+    const unsigned int n0 = (unsigned int)(p1 >> 32) ^ c1 ^ k0, n1 = (unsigned int)p1;
+    const unsigned int n2 = (unsigned int)(p0 >> 32) ^ c3 ^ k1, n3 = (unsigned int)p0;
+    c0 = n0;
+    c1 = n1;
+    c2 = n2;
+    c3 = n3;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+/* The random byte of element (query i, key j) of head bh. */
+int oracle_dropout_byte(unsigned long long seed, unsigned int offset, int bh, int i, int j) {
+  const unsigned int ctr[4] = {(unsigned int)j >> 2, (unsigned int)i >> 2, (unsigned int)bh, offset};
+  const unsigned int key[2] = {(unsigned int)(seed & 0xFFFFFFFFull), (unsigned int)(seed >> 32)};
+  unsigned int out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  return (int)((out[i & 3] >> (8 * (j & 3))) & 0xFFu);
+}
+
+/* Z_ij: 0 if the element is dropped, else 256 / (256 - p256). */
+static double drop_factor(unsigned long long seed, unsigned int offset, int bh, int i, int j, int p256) {
+  return oracle_dropout_byte(seed, offset, bh, i, j) >= p256 ? 256.0 / (256.0 - p256) : 0.0;
+}
+
+/* Forward with dropout, self-attention (N query rows and keys); rows as in oracle_fwd. */
+int oracle_fwd_drop(const double* q, const double* k, const double* v, double* o, double* lse, int BH, int N, int d,
+                    double scale, int causal, int p256, unsigned long long seed, unsigned int offset, const int* rows,
+                    int nrows, int nthreads) {
+  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !lse || p256 < 0 || p256 > 255) return -1;
+  if (!rows) nrows = N;
+  for (int r = 0; rows && r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return -1;
+  set_threads(nthreads);
+  int failed = 0;
+  const long long total = (long long)BH * nrows;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long long w = 0; w < total; ++w) {
+      if (!s) continue;
+      const int h = (int)(w / nrows);
+      const int i = rows ? rows[w % nrows] : (int)(w % nrows);
+      const double* qi = q + ((size_t)h * N + i) * d;
+      const double* kh = k + (size_t)h * N * d;
+      const double* vh = v + (size_t)h * N * d;
+      double* oi = o + ((size_t)h * N + i) * d;
+      const int n_vis = causal ? i + 1 : N;
+      double M, l;
+      score_row(qi, kh, n_vis, d, scale, s, &M, &l);
+      for (int t = 0; t < d; ++t) oi[t] = 0.0;
+      for (int j = 0; j < n_vis; ++j) {
+        const double pz = exp(s[j] - M) / l * drop_factor(seed, offset, h, i, j, p256);
+        const double* vj = vh + (size_t)j * d;
+        for (int t = 0; t < d; ++t) oi[t] += pz * vj[t];
+      }
+      lse[(size_t)h * N + i] = M + log(l);
+    }
+    free(s);
+  }
+  return failed ? -1 : 0;
+}
+
+/* Backward with dropout, self-attention: dq, dk, dv for every row and key; D if non-NULL. */
+int oracle_bwd_drop(const double* q, const double* k, const double* v, const double* dO, double* dq, double* dk,
+                    double* dv, double* D, int BH, int N, int d, double scale, int causal, int p256,
+                    unsigned long long seed, unsigned int offset, int nthreads) {
+  if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !dO || !dq || !dk || !dv || p256 < 0 || p256 > 255) return -1;
+  set_threads(nthreads);
+  double* lse_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  double* D_all = (double*)malloc(sizeof(double) * (size_t)BH * N);
+  if (!lse_all || !D_all) {
+    free(lse_all);
+    free(D_all);
+    return -1;
+  }
+  int failed = 0;
+  /* Pass 1, per query row: P, the dropped dP, D, dS; dq. */
+  const long long total_rows = (long long)BH * N;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s || !dp) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (long long w = 0; w < total_rows; ++w) {
+      if (!s || !dp) continue;
+      const int h = (int)(w / N), i = (int)(w % N);
+      const size_t hb = (size_t)h * N * d;
+      const double* qi = q + hb + (size_t)i * d;
+      const double* dOi = dO + hb + (size_t)i * d;
+      const int n_vis = causal ? i + 1 : N;
+      double M, l;
+      score_row(qi, k + hb, n_vis, d, scale, s, &M, &l);
+      double Dsum = 0.0;
+      for (int j = 0; j < n_vis; ++j) {
+        s[j] = exp(s[j] - M) / l; /* P_ij */
+        dp[j] = drop_factor(seed, offset, h, i, j, p256) * dot(dOi, v + hb + (size_t)j * d, d);
+        Dsum += s[j] * dp[j];
+      }
+      lse_all[w] = M + log(l);
+      D_all[w] = Dsum;
+      double* dq_row = dq + hb + (size_t)i * d;
+      for (int t = 0; t < d; ++t) dq_row[t] = 0.0;
+      for (int j = 0; j < n_vis; ++j) {
+        const double ds = s[j] * (dp[j] - Dsum);
+        const double* kj = k + hb + (size_t)j * d;
+        for (int t = 0; t < d; ++t) dq_row[t] += scale * ds * kj[t];
+      }
+    }
+    free(s);
+    free(dp);
+  }
+  /* Pass 2, per key: dk and dv over the rows that see it. */
+  if (!failed) {
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long w = 0; w < total_rows; ++w) {
+      const int h = (int)(w / N), j = (int)(w % N);
+      const size_t hb = (size_t)h * N * d;
+      const double* kj = k + hb + (size_t)j * d;
+      const double* vj = v + hb + (size_t)j * d;
+      double* dkj = dk + hb + (size_t)j * d;
+      double* dvj = dv + hb + (size_t)j * d;
+      for (int t = 0; t < d; ++t) {
+        dkj[t] = 0.0;
+        dvj[t] = 0.0;
+      }
+      for (int i = causal ? j : 0; i < N; ++i) {
+        const double* qi = q + hb + (size_t)i * d;
+        const double* dOi = dO + hb + (size_t)i * d;
+        const double p = exp(scale * dot(qi, kj, d) - lse_all[(size_t)h * N + i]);
+        const double z = drop_factor(seed, offset, h, i, j, p256);
+        const double ds = p * (z * dot(dOi, vj, d) - D_all[(size_t)h * N + i]);
+        for (int t = 0; t < d; ++t) {
+          dkj[t] += scale * qi[t] * ds;
+          dvj[t] += p * z * dOi[t];
+        }
+      }
+    }
+  }
+  if (D && !failed) memcpy(D, D_all, sizeof(double) * (size_t)BH * N);
+  free(lse_all);
+  free(D_all);
+  return failed ? -1 : 0;
+}

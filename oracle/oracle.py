@@ -24,7 +24,8 @@ Arrays are numpy float64 of shape [BH, N, d] (lse and D: [BH, N]). The
 row sees every key as in a decoding step, and ``merge_partials`` combines the
 results of disjoint key ranges with the logsumexp form of the chapter-08
 update rule. ``fwd_fp8`` is the 8-bit forward (E4M3 inputs with one scale
-per tensor, probabilities rounded to E4M3 for the second product).
+per tensor, probabilities rounded to E4M3 for the second product);
+``fwd_drop`` / ``bwd_drop`` add dropout with a Philox4x32-10 mask.
 """
 from __future__ import annotations
 
@@ -84,6 +85,18 @@ def load(path: str | None = None):
         lib.oracle_fwd_fp8.argtypes = [u8p, u8p, u8p, c_double, c_double, c_double, dp, dp, c_int, c_int, c_int,
                                        c_double, c_int, c_int, ip, c_int, c_int]
         lib.oracle_fwd_fp8.restype = c_int
+        u32p = ctypes.POINTER(ctypes.c_uint)
+        c_u64, c_u32 = ctypes.c_ulonglong, ctypes.c_uint
+        lib.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_dropout_byte.argtypes = [c_u64, c_u32, c_int, c_int, c_int]
+        lib.oracle_dropout_byte.restype = c_int
+        lib.oracle_fwd_drop.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, c_int, c_u64, c_u32,
+                                        ip, c_int, c_int]
+        lib.oracle_fwd_drop.restype = c_int
+        lib.oracle_bwd_drop.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, c_int,
+                                        c_u64, c_u32, c_int]
+        lib.oracle_bwd_drop.restype = c_int
         lib.oracle_max_threads.argtypes = [c_int]
         lib.oracle_max_threads.restype = c_int
         if path is None:
@@ -269,6 +282,53 @@ def fwd_fp8(q8, k8, v8, desc_q: float, desc_k: float, desc_v: float, scale: floa
     if rc != 0:
         raise RuntimeError("oracle_fwd_fp8 failed")
     return o, lse
+
+
+def philox4x32_10(ctr, key, lib=None):
+    """Philox4x32-10 of a 4-word counter and a 2-word key: 4 output words."""
+    lib = lib or load()
+    arr = ctypes.c_uint * 4
+    c, k, out = arr(*[int(x) & 0xFFFFFFFF for x in ctr]), (ctypes.c_uint * 2)(*[int(x) & 0xFFFFFFFF for x in key]), arr()
+    lib.oracle_philox4x32_10(c, k, out)
+    return [int(x) for x in out]
+
+
+def dropout_byte(seed: int, offset: int, bh: int, i: int, j: int, lib=None) -> int:
+    """The random byte of element (query i, key j) of head bh; kept iff byte >= p256."""
+    return int((lib or load()).oracle_dropout_byte(int(seed), int(offset), int(bh), int(i), int(j)))
+
+
+def fwd_drop(q, k, v, scale: float, causal: bool, p256: int, seed: int, offset: int = 0, rows=None,
+             nthreads: int = 0, lib=None):
+    """Forward with dropout of probability p256 / 256 after the softmax (self-attention). Returns (o, lse)."""
+    lib = lib or load()
+    q3, k3, v3 = (_as3(_f64(x)) for x in (q, k, v))
+    BH, N, d = q3.shape
+    o = np.full_like(q3, np.nan)
+    lse = np.full((BH, N), np.nan)
+    ridx, nr = _iptr(rows)
+    rc = lib.oracle_fwd_drop(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(o), _dptr(lse), BH, N, d, float(scale),
+                             int(causal), int(p256), int(seed), int(offset),
+                             None if ridx is None else ridx.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nr,
+                             nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_fwd_drop failed")
+    return o, lse
+
+
+def bwd_drop(q, k, v, dO, scale: float, causal: bool, p256: int, seed: int, offset: int = 0, nthreads: int = 0,
+             lib=None):
+    """Backward with the same dropout mask as fwd_drop. Returns (dq, dk, dv, D)."""
+    lib = lib or load()
+    q3, k3, v3, d3 = (_as3(_f64(x)) for x in (q, k, v, dO))
+    BH, N, d = q3.shape
+    dq, dk, dv = (np.full_like(q3, np.nan) for _ in range(3))
+    D = np.full((BH, N), np.nan)
+    rc = lib.oracle_bwd_drop(_dptr(q3), _dptr(k3), _dptr(v3), _dptr(d3), _dptr(dq), _dptr(dk), _dptr(dv), _dptr(D),
+                             BH, N, d, float(scale), int(causal), int(p256), int(seed), int(offset), nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_bwd_drop failed")
+    return dq, dk, dv, D
 
 
 def _mask(N: int, causal: bool) -> np.ndarray:

@@ -440,6 +440,108 @@ def pin_fp8_rounding_brute_force(lib=None):
                 assert np.allclose(o[h, i], (p[:, None] * v[h, :n]).sum(axis=0) / w.sum(), rtol=0, atol=1e-12)
 
 
+def _philox(ctr, key, width, mult, weyl, rounds=10):
+    """Philox-4xW (Salmon, Moraes, Dror and Shaw, SC 2011), written from the paper's round function."""
+    mask = (1 << width) - 1
+    c, k = list(ctr), list(key)
+    for _ in range(rounds):
+        p0, p1 = mult[0] * c[0], mult[1] * c[2]
+        c = [(p1 >> width) ^ c[1] ^ k[0], p1 & mask, (p0 >> width) ^ c[3] ^ k[1], p0 & mask]
+        k = [(k[0] + weyl[0]) & mask, (k[1] + weyl[1]) & mask]
+    return c
+
+
+_PHILOX32 = dict(width=32, mult=(0xD2511F53, 0xCD9E8D57), weyl=(0x9E3779B9, 0xBB67AE85))
+
+
+def _drop_byte(seed, offset, bh, i, j):
+    out = _philox([j >> 2, i >> 2, bh, offset], [seed & 0xFFFFFFFF, seed >> 32], **_PHILOX32)
+    return (out[i & 3] >> (8 * (j & 3))) & 0xFF
+
+
+def pin_philox(lib=None):
+    """The round structure equals numpy's Philox4x64-10 (a library generator; numpy advances its counter
+    before the first block), and the oracle's Philox4x32-10 equals the published known-answer vectors of
+    the generator's reference implementation and this structure on random counters and keys."""
+    w64 = dict(width=64, mult=(0xD2E7470EE14C6C93, 0xCA5A826395121157), weyl=(0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B))
+    for key in (0, 12345, 2 ** 63 + 7):
+        raw = np.random.Philox(key=key).random_raw(8)
+        assert [int(x) for x in raw[:4]] == _philox([1, 0, 0, 0], [key, 0], **w64)
+        assert [int(x) for x in raw[4:]] == _philox([2, 0, 0, 0], [key, 0], **w64)
+    kat = [(([0, 0, 0, 0], [0, 0]), [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+           (([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2), [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+           (([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0]),
+            [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1])]
+    for (ctr, key), want in kat:
+        assert orc.philox4x32_10(ctr, key, lib=lib) == want
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        ctr, key = [int(x) for x in rng.integers(0, 2 ** 32, 4)], [int(x) for x in rng.integers(0, 2 ** 32, 2)]
+        assert orc.philox4x32_10(ctr, key, lib=lib) == _philox(ctr, key, **_PHILOX32)
+    for (bh, i, j) in ((0, 0, 0), (3, 17, 250), (1, 4095, 4094), (127, 1000, 5)):
+        assert orc.dropout_byte(0x1234ABCD5678, 9, bh, i, j, lib=lib) == _drop_byte(0x1234ABCD5678, 9, bh, i, j)
+
+
+def pin_dropout_zero_is_plain(lib=None):
+    """p = 0 keeps every element with factor 1: dropout forward and backward equal the plain ones."""
+    q, k, v, dO = _qkv(210, 2, 21, 8)
+    for causal in (False, True):
+        a, b = orc.fwd_drop(q, k, v, 0.4, causal, 0, 99, lib=lib), orc.fwd(q, k, v, 0.4, causal, lib=lib)
+        assert np.allclose(a[0], b[0], rtol=0, atol=1e-14) and np.allclose(a[1], b[1], rtol=0, atol=1e-14)
+        ga, gb = orc.bwd_drop(q, k, v, dO, 0.4, causal, 0, 99, lib=lib), orc.bwd(q, k, v, dO, 0.4, causal, lib=lib)
+        assert all(np.allclose(x, y, rtol=0, atol=1e-13) for x, y in zip(ga, gb))
+
+
+def pin_dropout_keep_rate(lib=None):
+    """The random bytes are uniform: for each threshold the kept share is within 5 sigma of (256 - p256) / 256."""
+    lib = lib or orc.load()
+    b = np.array([orc.dropout_byte(77, 3, bh, i, j, lib=lib) for bh in range(2) for i in range(64) for j in range(96)])
+    n = b.size
+    for t in (1, 26, 128, 230, 255):
+        p = (256 - t) / 256
+        assert abs((b >= t).mean() - p) <= 5 * math.sqrt(p * (1 - p) / n), t
+    hist = np.bincount(b, minlength=256)
+    chi2 = float(((hist - n / 256) ** 2 / (n / 256)).sum())
+    assert chi2 < 255 + 6 * math.sqrt(2 * 255)  # 255 degrees of freedom
+
+
+def pin_dropout_brute_force(lib=None):
+    """A tiny dropout forward with numpy and the mask from the Philox structure above:
+    o_i = sum_j softmax_j * [byte_ij >= p256] * 256 / (256 - p256) * v_j; lse as without dropout."""
+    BH, N, d, p256, seed, off = 2, 9, 4, 77, 0xDEADBEEF01, 5
+    q, k, v, _ = _qkv(220, BH, N, d)
+    for causal in (False, True):
+        o, lse = orc.fwd_drop(q, k, v, 0.5, causal, p256, seed, off, lib=lib)
+        for h in range(BH):
+            for i in range(N):
+                n = i + 1 if causal else N
+                s = 0.5 * k[h, :n] @ q[h, i]
+                p = np.exp(s - s.max()) / np.exp(s - s.max()).sum()
+                z = np.array([(_drop_byte(seed, off, h, i, j) >= p256) * 256 / (256 - p256) for j in range(n)])
+                assert np.allclose(o[h, i], (p * z) @ v[h, :n], rtol=0, atol=1e-12)
+                assert abs(lse[h, i] - (s.max() + math.log(np.exp(s - s.max()).sum()))) < 1e-12
+
+
+def pin_dropout_gradients(lib=None):
+    """With the mask fixed by (seed, offset), the dropout forward is a smooth function of q, k, v: its
+    central finite differences give the backward's dq, dk, dv; and D_i = dO_i . o_i still holds."""
+    BH, N, d, p256, seed = 1, 7, 3, 90, 31337
+    q, k, v, dO = _qkv(230, BH, N, d)
+    for causal in (False, True):
+        dq, dk, dv, D = orc.bwd_drop(q, k, v, dO, 0.6, causal, p256, seed, lib=lib)
+        o, _ = orc.fwd_drop(q, k, v, 0.6, causal, p256, seed, lib=lib)
+        assert np.allclose(D, (dO * o).sum(axis=-1), rtol=0, atol=1e-12)
+        eps = 1e-6
+        for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+            for idx in [(0, 0, 0), (0, 3, 1), (0, N - 1, d - 1), (0, 5, 2)]:
+                xs = [q.copy(), k.copy(), v.copy()]
+                xs[which][idx] += eps
+                lp = (orc.fwd_drop(*xs, 0.6, causal, p256, seed, lib=lib)[0] * dO).sum()
+                xs[which][idx] -= 2 * eps
+                lm = (orc.fwd_drop(*xs, 0.6, causal, p256, seed, lib=lib)[0] * dO).sum()
+                assert abs((lp - lm) / (2 * eps) - grad[idx]) < 1e-6, (which, idx)
+
+
 ALL_PINS = [
     pin_zero_q_noncausal,
     pin_zero_q_causal,
@@ -465,4 +567,9 @@ ALL_PINS = [
     pin_fp8_unrounded_is_exact_attention,
     pin_fp8_zero_q,
     pin_fp8_rounding_brute_force,
+    pin_philox,
+    pin_dropout_zero_is_plain,
+    pin_dropout_keep_rate,
+    pin_dropout_brute_force,
+    pin_dropout_gradients,
 ]

@@ -38,6 +38,13 @@ MUTANTS = [
     ("fp8_dropped_v_scale", "oi[t] += pj * desc_v * oracle_e4m3_decode(vrow[t]);",
      "oi[t] += pj * oracle_e4m3_decode(vrow[t]);"),
     ("fp8_causal_skips_diagonal", "const int n = causal ? i + 1 : N;", "const int n = causal ? i : N;"),
+    ("philox_nine_rounds", "for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
+    ("dropout_mask_transposed", "{(unsigned int)j >> 2, (unsigned int)i >> 2, (unsigned int)bh, offset}",
+     "{(unsigned int)i >> 2, (unsigned int)j >> 2, (unsigned int)bh, offset}"),
+    ("dropout_unscaled", "? 256.0 / (256.0 - p256) : 0.0;", "? 1.0 : 0.0;"),
+    ("dropout_dv_unmasked", "dvj[t] += p * z * dOi[t];", "dvj[t] += p * dOi[t];"),
+    ("dropout_dp_unmasked", "dp[j] = drop_factor(seed, offset, h, i, j, p256) * dot(dOi, v + hb + (size_t)j * d, d);",
+     "dp[j] = dot(dOi, v + hb + (size_t)j * d, d);"),
     ("dp_uses_o_index", "dp[j] = dot(dOi, v + kb + (size_t)j * d, d);", "dp[j] = dot(dOi, v + kb + (size_t)i * d, d);"),
 ]
 
