@@ -13,6 +13,7 @@
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "philox.cuh"
 
 namespace {
 
@@ -207,6 +208,41 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, flo
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, int p256, unsigned long long seed, unsigned int offset, void* stream) {
+  if (!q || !k || !v || !o || !lse || p256 < 0 || p256 > 255) return FA_ERR_INVALID_ARG;
+  int st = check_shape(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const int BH = B * H;
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, 64, 128))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.status = di->status;
+  a.BH = BH;
+  a.H = H;
+  a.Nq = N;
+  a.Nk = N;
+  a.d = d;
+  a.scale_log2 = (float)((double)scale * kLog2e);
+  a.o_scale = (float)(256.0 / (256.0 - p256));  // kept elements carry 1 / (1 - p)
+  a.causal = causal ? 1 : 0;
+  a.drop_p256 = p256;
+  a.drop_offset = offset;
+  fa::philox::round_keys(seed, a.drop_rk);
+  a.split_blocks = (N + 127) / 128;
+  a.n_split = 1;
+  return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) { return fa_bwd_kv_workspace_bytes(B, H, N, N, d); }
 
 size_t fa_bwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -222,9 +258,36 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                    workspace_bytes, stream);
 }
 
+namespace {
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+               const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
+               void* workspace, size_t workspace_bytes, void* stream);
+}  // namespace
+
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int p256,
+                   unsigned long long seed, unsigned int offset, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (p256 < 0 || p256 > 255) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, nullptr, nullptr, p256, seed,
+                    offset, workspace, workspace_bytes, stream);
+}
+
 int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
               const int* seqlens_q, const int* seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, seqlens_q, seqlens_k, 0, 0, 0,
+                    workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+               const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
+               void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int st = check_shape(B, H, Nq, d, scale);
   if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
@@ -265,8 +328,15 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const 
   a.causal = causal ? 1 : 0;
   a.seqlens_q = seqlens_q;
   a.seqlens_k = seqlens_k;
+  a.drop_p256 = p256;
+  a.drop_offset = offset;
+  a.drop_scale = (float)(256.0 / (256.0 - p256));
+  fa::philox::round_keys(seed, a.drop_rk);
   return fa::launch_bwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
+}  // namespace
+
+extern "C" {
 
 const char* fa_status_string(int status) {
   switch (status) {

@@ -37,6 +37,7 @@
 
 #include "fa_internal.h"
 #include "block_order.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -176,7 +177,8 @@ __device__ __forceinline__ DkdvTile dkdv_tile(int L, const BwdArgs& a, int nkv) 
   return t;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+// DROP: the forward's dropout mask, made again from the seed (philox.cuh).
+template <int D, bool CAUSAL, bool VARLEN, bool DROP = false>
 __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -632,6 +634,23 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
             }
           }
         }
+        // dropout: keep bytes kw[gq], byte b for query q0 + 64 w + 4 gq + b of this thread's key. Each
+        // call covers 4 queries x the quad's 4 keys; this lane draws query groups qa, qa + 4, .. and the
+        // byte and quad transposes leave it its own key's bytes of all 16 groups.
+        uint32_t kw[DROP ? 16 : 1];
+        if constexpr (DROP) {
+          const uint32_t i4 = (uint32_t)(q0 + 64 * w) >> 2, j4 = (uint32_t)key >> 2, qa = lane & 3;
+          const uint32_t thr4 = (uint32_t)a.drop_p256 * 0x01010101u;
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            uint32_t x[4];
+            philox::philox4x32_10(j4, i4 + 4 * n + qa, (uint32_t)t.bh, a.drop_offset, a.drop_rk, x);
+            philox::byte_transpose(x);  // x[b]: key 4 j4 + b, the group's 4 queries
+            philox::quad_transpose(x);  // x[s]: this lane's key, query group 4 n + s
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) kw[4 * n + s4] = philox::keep_bytes(x[s4], thr4);
+          }
+        }
         ok = mbar_wait(&bars.dp_full, g & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -650,17 +669,31 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
             const int col = 32 * h + c;
             const float4 nd = rb4[16 + (col >> 2)];  // -D
             const uint32_t pa = pk[col >> 1], pb = pk[(col >> 1) + 1];
-            const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)),
-                                     fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                           make_float2(nd.x, nd.y)));
-            const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)),
-                                     fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
-                                           make_float2(nd.z, nd.w)));
+            const float2 dp01 = make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
+            const float2 dp23 = make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3]));
+            float2 e01, e23;  // dP - D, with dropout Z dP - D (Z = 0 or 1 / (1 - p))
+            if constexpr (DROP) {
+              const uint32_t kc = kw[col >> 2];
+              const float f = a.drop_scale;
+              e01 = ffma2(dp01, make_float2(philox::keep_factor(kc, 0, f), philox::keep_factor(kc, 1, f)),
+                          make_float2(nd.x, nd.y));
+              e23 = ffma2(dp23, make_float2(philox::keep_factor(kc, 2, f), philox::keep_factor(kc, 3, f)),
+                          make_float2(nd.z, nd.w));
+            } else {
+              e01 = fadd2(dp01, make_float2(nd.x, nd.y));
+              e23 = fadd2(dp23, make_float2(nd.z, nd.w));
+            }
+            const float2 d01 = fmul2(make_float2(__uint_as_float(pa << 16), __uint_as_float(pa & 0xFFFF0000u)), e01);
+            const float2 d23 = fmul2(make_float2(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u)), e23);
             dsk[c >> 1] = pack_bf16x2(d01.x, d01.y);
             dsk[(c >> 1) + 1] = pack_bf16x2(d23.x, d23.y);
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pkh[i] = pk[16 * h + i];
+          for (int i = 0; i < 16; ++i) {
+            pkh[i] = pk[16 * h + i];
+            if constexpr (DROP)  // the dropped P^T feeds dV (pair 16 h + i: queries 32 h + 2 i, + 1)
+              pkh[i] &= (i & 1) ? philox::pair_mask_hi(kw[(16 * h + i) >> 1]) : philox::pair_mask_lo(kw[(16 * h + i) >> 1]);
+          }
           tmem_st16(t_dp + 32 * h, pkh);       // P^T of these queries
           tmem_st16(t_dp + 32 * h + 16, dsk);  // dS^T of these queries
           tmem_st_wait();
@@ -679,7 +712,8 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dkdv_kernel(const __grid_consta
         tc_fence_after();
         uint8_t* stage = w == 0 ? smem + C::kOffDO + (g_last % C::kDOStages) * C::kTileBytes
                                 : smem + C::kOffQ + (g_last % C::kQStages) * C::kTileBytes;
-        stage_row_bf16<D>(tmem + lane_off + (w == 0 ? C::kColDV : C::kColDK), stage, r, 0, w == 0 ? 1.f : a.scale);
+        stage_row_bf16<D>(tmem + lane_off + (w == 0 ? C::kColDV : C::kColDK), stage, r, 0,
+                          w == 0 ? (DROP ? a.drop_scale : 1.f) : a.scale);
         fence_proxy_async_smem();
       }
       tc_fence_before();
@@ -786,7 +820,7 @@ __device__ __forceinline__ DqTile dq_tile(int L, const BwdArgs& a, int nq) {
   return t;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool DROP = false>
 __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1163,6 +1197,21 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
             }
           }
         }
+        // dropout: keep bytes kw[gk], byte b for key k0 + 4 gk + b of this thread's query. This lane
+        // draws key groups qa, qa + 4, .. for the quad's 4 queries; the quad exchange leaves it its row's.
+        uint32_t kw[DROP ? 16 : 1];
+        if constexpr (DROP) {
+          const uint32_t j4 = (uint32_t)k0 >> 2, i4 = (uint32_t)q >> 2, qa = lane & 3;
+          const uint32_t thr4 = (uint32_t)a.drop_p256 * 0x01010101u;
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            uint32_t x[4];
+            philox::philox4x32_10(j4 + 4 * n + qa, i4, (uint32_t)t.bh, a.drop_offset, a.drop_rk, x);
+            philox::quad_transpose(x);  // x[s]: this lane's query, key group 4 n + s
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) kw[4 * n + s4] = philox::keep_bytes(x[s4], thr4);
+          }
+        }
         ok = mbar_wait(&bars.dp_full, gj & 1, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -1182,9 +1231,18 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const int col = 32 * h + c;
-            // dS = P (dP - D)
-            const float2 d =
-                fmul2(pf[col >> 1], fadd2(make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1])), nd2));
+            // dS = P (dP - D), with dropout P (Z dP - D)
+            const float2 dpc = make_float2(__uint_as_float(dp[h][c]), __uint_as_float(dp[h][c + 1]));
+            float2 e;
+            if constexpr (DROP) {
+              const uint32_t kc = kw[col >> 2];
+              const int b = col & 3;
+              e = ffma2(dpc, make_float2(philox::keep_factor(kc, b, a.drop_scale), philox::keep_factor(kc, b + 1, a.drop_scale)),
+                        nd2);
+            } else {
+              e = fadd2(dpc, nd2);
+            }
+            const float2 d = fmul2(pf[col >> 1], e);
             dsk[col >> 1] = pack_bf16x2(d.x, d.y);
           }
         }
@@ -1290,6 +1348,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const bool varlen = a.seqlens_q || a.seqlens_k;
   auto kv = varlen ? fa_bwd_dkdv_kernel<D, CAUSAL, true> : fa_bwd_dkdv_kernel<D, CAUSAL, false>;
+  if (a.drop_p256 > 0) kv = fa_bwd_dkdv_kernel<D, CAUSAL, false, true>;  // dropout: no lengths
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
@@ -1298,6 +1357,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
   kv<<<(unsigned)std::min<long long>(kv_tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto kq = varlen ? fa_bwd_dq_kernel<D, CAUSAL, true> : fa_bwd_dq_kernel<D, CAUSAL, false>;
+  if (a.drop_p256 > 0) kq = fa_bwd_dq_kernel<D, CAUSAL, false, true>;
   if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;

@@ -25,6 +25,7 @@
 // arithmetic while most O rescales are skipped.
 #include "fa_internal.h"
 #include "block_order.cuh"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -92,8 +93,9 @@ __device__ inline void zero_rows(const FwdArgs& a, int bh, int r0, int n, int ti
 
 // VARLEN: per-sequence lengths are given (padding masks); without them the
 // lengths are the array sizes, which the kernel then takes as constants.
-// FP8: E4M3 inputs and 8-bit products (FwdCfg).
-template <int D, bool CAUSAL, bool VARLEN, bool FP8 = false>
+// FP8: E4M3 inputs and 8-bit products (FwdCfg). DROP: dropout of P after the
+// softmax with a Philox mask (philox.cuh); O / l takes the 1 / (1 - p) factor.
+template <int D, bool CAUSAL, bool VARLEN, bool FP8 = false, bool DROP = false>
 __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -428,6 +430,25 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
             sum = fadd2(sum, p);
             pk[c >> 1] = pack_bf16x2(p.x, p.y);
           }
+          if constexpr (DROP) {
+            // keys kv0 + 32 ch + [0, 32) are 8 groups of 4: this lane draws groups qa and qa + 4 for
+            // the quad's 4 rows, and the quad exchange leaves it its own row's bytes of all 8
+            const uint32_t j4 = (uint32_t)(kv0 + 32 * ch) >> 2, i4 = (uint32_t)row >> 2, qa = lane & 3;
+            const uint32_t thr4 = (uint32_t)a.drop_p256 * 0x01010101u;
+            uint32_t x0[4], x1[4];
+            philox::philox4x32_10(j4 + qa, i4, (uint32_t)bh, a.drop_offset, a.drop_rk, x0);
+            philox::philox4x32_10(j4 + qa + 4, i4, (uint32_t)bh, a.drop_offset, a.drop_rk, x1);
+            philox::quad_transpose(x0);
+            philox::quad_transpose(x1);
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {  // x0[s4]: keys 4 s4 .. + 3 of the chunk; x1[s4]: 16 + 4 s4 ..
+              const uint32_t k0m = philox::keep_bytes(x0[s4], thr4), k1m = philox::keep_bytes(x1[s4], thr4);
+              pk[2 * s4] &= philox::pair_mask_lo(k0m);
+              pk[2 * s4 + 1] &= philox::pair_mask_hi(k0m);
+              pk[8 + 2 * s4] &= philox::pair_mask_lo(k1m);
+              pk[8 + 2 * s4 + 1] &= philox::pair_mask_hi(k1m);
+            }
+          }
           tmem_st16(t_s + 16 * ch, pk);
         }
       }
@@ -560,6 +581,7 @@ __global__ void __launch_bounds__(256) fa_fwd_merge_kernel(const __grid_constant
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   auto kern = a.seqlens_q || a.seqlens_k ? fa_fwd_kernel<D, CAUSAL, true> : fa_fwd_kernel<D, CAUSAL, false>;
+  if (a.drop_p256 > 0) kern = fa_fwd_kernel<D, CAUSAL, false, false, true>;  // dropout: no lengths, no key ranges
   int smem = FwdCfg<D>::kSmemBytes;
   if constexpr (D == 128) {
     if (a.fp8) {  // 8-bit inputs: no lengths, no key ranges

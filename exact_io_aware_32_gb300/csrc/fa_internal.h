@@ -23,6 +23,11 @@ struct FwdArgs {
   // its first seq_len(seqlens_q, b, Nq) query rows and seq_len(seqlens_k, b, Nk) keys
   const int* seqlens_q;
   const int* seqlens_k;
+  // dropout of P after the softmax (probability drop_p256 / 256; 0: none):
+  // Philox4x32-10 round keys of the seed, the counter's fourth word
+  int drop_p256;
+  unsigned int drop_offset;
+  unsigned int drop_rk[20];
   int head_group;    // heads per CTA scheduling group (set by launch_fwd)
   // Key ranges per query block. With n_split > 1, CTA z covers key blocks
   // [z * split_blocks, (z + 1) * split_blocks) and writes O / l (fp32) and the
@@ -48,6 +53,10 @@ struct BwdArgs {
   int causal;         // query row i sees keys 0 .. i + Nk - Nq (needs Nq <= Nk)
   const int* seqlens_q;  // optional per-sequence lengths, as in FwdArgs
   const int* seqlens_k;
+  int drop_p256;          // dropout, as in FwdArgs (the forward's seed and offset)
+  unsigned int drop_offset;
+  unsigned int drop_rk[20];
+  float drop_scale;       // 256 / (256 - drop_p256)
   int head_group;     // heads per CTA scheduling group of the dK/dV kernel (set by launch_bwd)
   int head_group_dq;  // the same for the dQ kernel
 };

@@ -2,11 +2,12 @@
 
 Argument marshalling only: every step of attention runs in the CUDA kernels
 of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
-``fa_fwd_kv_workspace_bytes``, ``fa_fwd_fp8``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
+``fa_fwd_kv_workspace_bytes``, ``fa_fwd_fp8``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
 ``fa_bwd_kv_workspace_bytes``,
 ``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
 torch CUDA tensors or raw device addresses (ints). ``forward``,
-``forward_kv``, ``forward_fp8``, ``backward`` and ``backward_kv`` are conveniences that
+``forward_kv``, ``forward_fp8``, ``forward_dropout``, ``backward``, ``backward_kv`` and
+``backward_dropout`` are conveniences that
 allocate the outputs with torch.
 
 If the library has not been built, or cannot be loaded, every call raises:
@@ -29,8 +30,9 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_TIMEOUT = 6
 
-EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
-            "fa_bwd_kv", "fa_bwd_kv_workspace_bytes", "fa_status_string", "fa_device_status", "fa_bwd_noalloc")
+EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_fwd_fp8", "fa_fwd_dropout", "fa_bwd",
+            "fa_bwd_workspace_bytes", "fa_bwd_kv", "fa_bwd_kv_workspace_bytes", "fa_bwd_dropout", "fa_status_string",
+            "fa_device_status", "fa_bwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +70,13 @@ def load(path: str | None = None):
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, c_float, c_float, c_float, vp, vp, c_int, c_int, c_int, c_int, c_float,
                                    c_int, vp]
         lib.fa_fwd_fp8.restype = c_int
+        c_u64, c_u32 = ctypes.c_ulonglong, ctypes.c_uint
+        lib.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int, c_int, c_u64,
+                                       c_u32, vp]
+        lib.fa_fwd_dropout.restype = c_int
+        lib.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_float, c_int,
+                                       c_int, c_u64, c_u32, vp, c_size_t, vp]
+        lib.fa_bwd_dropout.restype = c_int
         lib.fa_fwd_kv_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int, c_int]
         lib.fa_fwd_kv_workspace_bytes.restype = c_size_t
         lib.fa_bwd_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
@@ -131,6 +140,19 @@ def fa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, o,
                scale: float, causal: bool, stream=None) -> int:
     return int(load().fa_fwd_fp8(_addr(q), _addr(k), _addr(v), float(descale_q), float(descale_k), float(descale_v),
                                  _addr(o), _addr(lse), B, H, N, d, float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fa_fwd_dropout(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool, p256: int, seed: int,
+                   offset: int = 0, stream=None) -> int:
+    return int(load().fa_fwd_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), B, H, N, d, float(scale),
+                                     int(bool(causal)), int(p256), int(seed), int(offset), _stream(stream)))
+
+
+def fa_bwd_dropout(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                   p256: int, seed: int, offset: int, workspace, workspace_bytes: int, stream=None) -> int:
+    return int(load().fa_bwd_dropout(_addr(q), _addr(k), _addr(v), _addr(o), _addr(lse), _addr(dO), _addr(dq),
+                                     _addr(dk), _addr(dv), B, H, N, d, float(scale), int(bool(causal)), int(p256),
+                                     int(seed), int(offset), _addr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -207,6 +229,38 @@ def forward_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float
     if st != FA_OK:
         raise FAError(st, "fa_fwd_fp8")
     return o, lse
+
+
+def forward_dropout(q, k, v, p256: int, seed: int, offset: int = 0, causal: bool = False, scale: float | None = None,
+                    stream=None):
+    """Forward with dropout probability p256 / 256 (Philox mask of seed, offset). Returns (o, lse)."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, p256, seed, offset, stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_dropout")
+    return o, lse
+
+
+def backward_dropout(q, k, v, o, lse, dO, p256: int, seed: int, offset: int = 0, causal: bool = False,
+                     scale: float | None = None, stream=None):
+    """Backward of forward_dropout with the same (p256, seed, offset). Returns (dq, dk, dv)."""
+    import torch
+
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = fa_bwd_dropout(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, p256, seed, offset, ws, need,
+                        stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd_dropout")
+    return dq, dk, dv
 
 
 def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split: bool = True, seqlens_q=None,

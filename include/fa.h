@@ -226,6 +226,31 @@ FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const voi
                           const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                           int causal, void* stream);
 
+/*
+ * Forward and backward with dropout of P after the softmax ("FlashAttention
+ * and GPU Memory": chapter 07 fuses dropout into the one kernel; chapter 09's
+ * backward keeps only the generator's state and makes the mask again).
+ *   p256     dropout probability p256 / 256, 0 .. 255 (FA_ERR_INVALID_ARG
+ *            otherwise; 0 is the plain pass); kept elements are scaled by
+ *            256 / (256 - p256)
+ *   seed, offset
+ *            the mask: element (query i, key j) of head bh = b * H + h is kept
+ *            iff byte (j mod 4) of word (i mod 4) of Philox4x32-10 (Salmon,
+ *            Moraes, Dror and Shaw, SC 2011) with counter (j / 4, i / 4, bh,
+ *            offset) and key (seed mod 2^32, seed / 2^32) is >= p256. The same
+ *            (seed, offset) in fa_bwd_dropout gives the same mask.
+ * o = (P o Z) v with Z = kept / (1 - p); lse is that of the undropped scores
+ * (what the backward needs). Other arguments, layouts and errors as in
+ * fa_fwd / fa_bwd (self-attention, N query rows and keys).
+ */
+FA_API int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, float scale, int causal, int p256, unsigned long long seed, unsigned int offset,
+                          void* stream);
+FA_API int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                          int causal, int p256, unsigned long long seed, unsigned int offset, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 FA_API const char* fa_status_string(int status);
 

@@ -104,6 +104,38 @@ def test_fwd_kv_workspace_bytes_without_gpu_or_bad_shape(lib):
 
 
 @pytest.mark.parametrize("args,status", [
+    (dict(p256=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(p256=256), fa.FA_ERR_INVALID_ARG),
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_fwd_dropout_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=2, N=256, d=128, scale=0.1, causal=1, p256=26, seed=1, offset=0)
+    kw.update(args)
+    st = fa.fa_fwd_dropout(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["B"], kw["H"], kw["N"], kw["d"],
+                           kw["scale"], kw["causal"], kw["p256"], kw["seed"], kw["offset"], stream=0)
+    assert st == status
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(p256=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(p256=300), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(ws_bytes=100), fa.FA_ERR_WORKSPACE),
+])
+def test_bwd_dropout_rejects_bad_args(lib, args, status):
+    kw = dict(q=A, k=A, v=A, o=A, lse=A, dO=A, dq=A, dk=A, dv=A, B=1, H=1, N=16, d=64, scale=0.125, causal=1, p256=26,
+              seed=2 ** 63 + 5, offset=7, ws=A, ws_bytes=1 << 20)
+    kw.update(args)
+    st = fa.fa_bwd_dropout(kw["q"], kw["k"], kw["v"], kw["o"], kw["lse"], kw["dO"], kw["dq"], kw["dk"], kw["dv"],
+                           kw["B"], kw["H"], kw["N"], kw["d"], kw["scale"], kw["causal"], kw["p256"], kw["seed"],
+                           kw["offset"], kw["ws"], kw["ws_bytes"], stream=0)
+    assert st == status
+
+
+@pytest.mark.parametrize("args,status", [
     (dict(v=0), fa.FA_ERR_INVALID_ARG),
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
