@@ -19,6 +19,9 @@ decoding forward instead (fa_fwd_kv: Nq query rows against a resident cache of
 Nk keys and values, split over key ranges): a step is one call, and the metric
 is the HBM bandwidth of its algorithmic bytes.
 
+``--dropout P256`` runs the step with dropout of probability P256 / 256
+(fa_fwd_dropout, fa_bwd_dropout; a new Philox mask every step).
+
 ``--workload fp8_<B>_<H>_<N>_<causal|noncausal>`` measures the 8-bit forward
 (fa_fwd_fp8, d = 128, E4M3 q, k, v with per-tensor factors): a step is one
 call, and the metric is its matmul TFLOP/s against the 8-bit dense peak.
@@ -46,6 +49,7 @@ METRIC = "attention fwd and fwd+bwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 
 DECODE_METRIC = "decoding attention forward (fa_fwd_kv): GB/s of algorithmic HBM bytes (bf16, 1 GB300)"
 FP8_METRIC = "8-bit attention forward (fa_fwd_fp8, E4M3 inputs): TFLOP/s (1 GB300) and % of dense FP8 peak"
 DEFAULT_WORKLOAD = "d128_n4096_causal"
+DROPOUT_SEED = 0x5EED
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 L2_BYTES = 129e6
 
@@ -256,15 +260,30 @@ def run_gpu(args, w, causal: bool):
     stream = torch.cuda.current_stream(dev)
     sp = int(stream.cuda_stream)
 
-    def fwd():
-        st = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, sp)
+    p256 = args.dropout  # dropout probability p256 / 256; every step draws a new mask (offset = step)
+
+    def fwd_call(xq, xk, xv, xo, xlse, step):
+        if p256:
+            st = fa.fa_fwd_dropout(xq, xk, xv, xo, xlse, B, H, N, d, scale, causal, p256, DROPOUT_SEED, step, sp)
+        else:
+            st = fa.fa_fwd(xq, xk, xv, xo, xlse, B, H, N, d, scale, causal, sp)
         if st:
             raise fa.FAError(st, "fa_fwd")
 
-    def bwd():
-        st = fa.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, sp)
+    def bwd_call(xq, xk, xv, xo, xlse, xdo, xdq, xdk, xdv, step):
+        if p256:
+            st = fa.fa_bwd_dropout(xq, xk, xv, xo, xlse, xdo, xdq, xdk, xdv, B, H, N, d, scale, causal, p256,
+                                   DROPOUT_SEED, step, ws, ws_bytes, sp)
+        else:
+            st = fa.fa_bwd(xq, xk, xv, xo, xlse, xdo, xdq, xdk, xdv, B, H, N, d, scale, causal, ws, ws_bytes, sp)
         if st:
             raise fa.FAError(st, "fa_bwd")
+
+    def fwd(step=0):
+        fwd_call(q, k, v, o, lse, step)
+
+    def bwd(step=0):
+        bwd_call(q, k, v, o, lse, dO, dq, dk, dv, step)
 
     def barrier():
         if dist is not None:
@@ -294,11 +313,11 @@ def run_gpu(args, w, causal: bool):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for e0, e1, e2 in ev:
+    for step, (e0, e1, e2) in enumerate(ev):
         e0.record(stream)
-        fwd()
+        fwd(step)
         e1.record(stream)
-        bwd()
+        bwd(step)
         e2.record(stream)
     t_end.record(stream)
     barrier()
@@ -344,12 +363,8 @@ def run_gpu(args, w, causal: bool):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])  # step i-2's results have left these buffers
-        st = fa.fa_fwd(xq, xk, xv, xo, xlse, B, H, N, d, scale, causal, sp)
-        if st:
-            raise fa.FAError(st, "fa_fwd")
-        st = fa.fa_bwd(xq, xk, xv, xo, xlse, xdo, xdq, xdk, xdv, B, H, N, d, scale, causal, ws, ws_bytes, sp)
-        if st:
-            raise fa.FAError(st, "fa_bwd")
+        fwd_call(xq, xk, xv, xo, xlse, i)
+        bwd_call(xq, xk, xv, xo, xlse, xdo, xdq, xdk, xdv, i)
         ev_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[b])
@@ -378,7 +393,7 @@ def run_gpu(args, w, causal: bool):
     burst = peaks["bf16_tflops"]
     sustained = peaks.get("bf16_tflops_sustained", burst)
     achieved = f_bwd / bwd_s / 1e12
-    traffic = kernel_traffic("fa_bwd.cu", f"fa_bwd<{d},{str(causal).lower()}>")
+    traffic = None if p256 else kernel_traffic("fa_bwd.cu", f"fa_bwd<{d},{str(causal).lower()}>")
     result = {
         "metric": METRIC,
         "value": round(value / 1e12, 2),
@@ -394,8 +409,9 @@ def run_gpu(args, w, causal: bool):
         "data": "synthetic",
         "config": {
             "workload": args.workload, "B": B, "H": H, "N": N, "d": d, "causal": causal,
-            "scale": scale, "qk_mult": w.qk_mult,
-            "step": "fa_fwd then fa_bwd (O, lse, dq, dk, dv)",
+            "scale": scale, "qk_mult": w.qk_mult, "dropout_p256": p256,
+            "step": "fa_fwd then fa_bwd (O, lse, dq, dk, dv)" if not p256 else
+                    f"fa_fwd_dropout then fa_bwd_dropout, p = {p256}/256, Philox4x32-10 mask, a new offset every step",
             "parallelism": f"replicas over (batch, head): {world} x {B * H} heads",
             "l2": f"inputs larger than L2: {5 * B * H * N * d * 2 / 1e6:.0f} MB of bf16 tensors per step vs "
                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
@@ -733,6 +749,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--dropout", type=int, default=0, help="dropout probability p256 / 256 in the step (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=120.0, help="seconds for --impl reference")
