@@ -97,6 +97,58 @@ constexpr double kLog2e = 1.4426950408889634074;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The backward of every entry point: arguments validated, then D prep, dK/dV and dQ.
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+               const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int st = check_shape(B, H, Nq, d, scale);
+  if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
+  if (st != FA_OK) return st;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(seqlens_q) || !aligned4(seqlens_k))
+    return FA_ERR_MISALIGNED;
+  const size_t need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_WORKSPACE;
+  DeviceInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const int BH = B * H;
+  fa::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.Dsum = static_cast<float*>(workspace);
+  a.work = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + (need - 256));
+  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
+      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.status = di->status;
+  a.BH = BH;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.scale = scale;
+  a.scale_log2 = (float)((double)scale * kLog2e);
+  a.causal = causal ? 1 : 0;
+  a.seqlens_q = seqlens_q;
+  a.seqlens_k = seqlens_k;
+  a.drop_p256 = p256;
+  a.drop_offset = offset;
+  a.drop_scale = (float)(256.0 / (256.0 - p256));
+  fa::philox::round_keys(seed, a.drop_rk);
+  return fa::launch_bwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
@@ -258,13 +310,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                    workspace_bytes, stream);
 }
 
-namespace {
-int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-               const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
-               void* workspace, size_t workspace_bytes, void* stream);
-}  // namespace
-
 int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, int p256,
                    unsigned long long seed, unsigned int offset, void* workspace, size_t workspace_bytes,
@@ -280,63 +325,6 @@ int fa_bwd_kv(const void* q, const void* k, const void* v, const void* o, const 
   return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, seqlens_q, seqlens_k, 0, 0, 0,
                     workspace, workspace_bytes, stream);
 }
-
-}  // extern "C"
-
-namespace {
-int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-               void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-               const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
-               void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  int st = check_shape(B, H, Nq, d, scale);
-  if (st == FA_OK) st = check_shape(B, H, Nk, d, scale);
-  if (st != FA_OK) return st;
-  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first rows would see no key
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(seqlens_q) || !aligned4(seqlens_k))
-    return FA_ERR_MISALIGNED;
-  const size_t need = fa_bwd_kv_workspace_bytes(B, H, Nq, Nk, d);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return FA_ERR_WORKSPACE;
-  DeviceInfo* di = nullptr;
-  if ((st = device_info(&di)) != FA_OK) return st;
-  const int BH = B * H;
-  fa::BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.Dsum = static_cast<float*>(workspace);
-  a.work = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + (need - 256));
-  if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
-      !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
-      !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
-      !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
-      !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
-      !encode_3d(&a.tm_dk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
-      !encode_3d(&a.tm_dv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128))
-    return FA_ERR_LAUNCH;
-  a.o = o;
-  a.dO = dO;
-  a.lse = lse;
-  a.status = di->status;
-  a.BH = BH;
-  a.H = H;
-  a.Nq = Nq;
-  a.Nk = Nk;
-  a.d = d;
-  a.scale = scale;
-  a.scale_log2 = (float)((double)scale * kLog2e);
-  a.causal = causal ? 1 : 0;
-  a.seqlens_q = seqlens_q;
-  a.seqlens_k = seqlens_k;
-  a.drop_p256 = p256;
-  a.drop_offset = offset;
-  a.drop_scale = (float)(256.0 / (256.0 - p256));
-  fa::philox::round_keys(seed, a.drop_rk);
-  return fa::launch_bwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
-}
-}  // namespace
-
-extern "C" {
 
 const char* fa_status_string(int status) {
   switch (status) {
