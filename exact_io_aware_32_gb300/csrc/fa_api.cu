@@ -162,7 +162,7 @@ size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   if (check_shape(B, H, Nq, d, 1.0f) != FA_OK || check_shape(B, H, Nk, d, 1.0f) != FA_OK) return 0;
   DeviceInfo* di = nullptr;
   if (device_info(&di) != FA_OK) return 0;
-  const int n = fa::pick_key_splits(B * H, Nq, Nk, di->num_sms);
+  const int n = fa::pick_key_splits(B * H, Nq, Nk, di->num_sms * fa::fwd_ctas_per_sm(d), fa::fwd_rows_per_cta(d));
   if (n <= 1) return 0;
   const size_t rows = (size_t)n * B * H * Nq;
   return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
@@ -205,7 +205,8 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   // Key ranges: as many as help fill the GPU and fit the caller's workspace
   // (none without one); every range non-empty.
   const int nkv = (Nk + 127) / 128;
-  int n = workspace ? fa::pick_key_splits(BH, Nq, Nk, di->num_sms) : 1;
+  int n = workspace ? fa::pick_key_splits(BH, Nq, Nk, di->num_sms * fa::fwd_ctas_per_sm(d), fa::fwd_rows_per_cta(d))
+                    : 1;
   for (; n > 1; --n) {
     const size_t rows = (size_t)n * BH * Nq;
     if (align256(rows * d * sizeof(float)) + align256(rows * sizeof(float)) <= workspace_bytes) break;

@@ -55,21 +55,31 @@ struct FwdCfg {
   // a query tile's slot also stages that tile's bf16 O for the store
   static constexpr int kQSlotBytes = (kPanels > kOPanels ? kPanels : kOPanels) * kPanelBytes;
   static constexpr int kKStep = FP8 ? 32 : 16;   // K of one MMA instruction
+  // Query tiles per CTA. At d = 64 a CTA takes one tile (256 TMEM columns,
+  // under 113 KB of shared memory), so that two CTAs share an SM and one's
+  // loads and epilogue overlap the other's main loop; otherwise two tiles.
+  static constexpr int kTiles = D == 64 ? 1 : 2;
+  static constexpr int kCtasPerSm = 3 - kTiles;
+  static constexpr int kRows = 128 * kTiles;      // query rows per CTA
+  static constexpr uint32_t kTmemCols = kTiles == 2 ? 512u : 256u;
   // K of a block is released once both tiles' S have read it, V only once both
   // PV products have: V gets the deeper ring, so its load has more than one
   // block's time to land.
-  static constexpr int kKStages = FP8 ? 4 : (D == 128 ? 2 : 4);
-  static constexpr int kVStages = FP8 ? 4 : (D == 128 ? 3 : 4);
+  static constexpr int kKStages = FP8 ? 4 : 2;
+  static constexpr int kVStages = FP8 ? 4 : 3;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQSlotBytes;
+  static constexpr int kOffK = kOffQ + kTiles * kQSlotBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+  static_assert(kCtasPerSm == 1 || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit an SM's shared memory");
   // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 reuses its first 64,
   // as E4M3 its first 32) and O_t (fp32, D columns) for query tiles t = 0, 1.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128u; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
-  static constexpr int kThreads = 320;
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 128u * kTiles + (uint32_t)t * D; }
+  // a softmax warpgroup per tile, then the TMA warp and the MMA warp
+  static constexpr int kThreads = 128 * kTiles + 64;
+  static constexpr int kWarpTma = 4 * kTiles, kWarpMma = 4 * kTiles + 1;
 };
 
 struct FwdBarriers {
@@ -96,7 +106,8 @@ __device__ inline void zero_rows(const FwdArgs& a, int bh, int r0, int n, int ti
 // FP8: E4M3 inputs and 8-bit products (FwdCfg). DROP: dropout of P after the
 // softmax with a Philox mask (philox.cuh); O / l takes the 1 / (1 - p) factor.
 template <int D, bool CAUSAL, bool VARLEN, bool FP8 = false, bool DROP = false>
-__global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCtasPerSm)
+    fa_fwd_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,12 +128,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   // this CTA's key blocks: [jb, je) (all of them unless the keys are split)
   const int jb = (int)blockIdx.z * a.split_blocks;
   const int je = min(nkv, jb + a.split_blocks);
-  int nb[2];  // key blocks each query tile sees in the range, from jb on
+  int nb[2];  // key blocks each query tile sees in the range, from jb on (none for an absent tile)
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int r0 = qblk * 256 + t * 128;
+    const int r0 = qblk * C::kRows + t * 128;
     const int last_key = CAUSAL ? min(min(r0 + 127, sq - 1) + off, sk - 1) : sk - 1;
-    nb[t] = r0 < sq ? max(0, min(last_key / C::BN + 1, je) - jb) : 0;
+    nb[t] = t < C::kTiles && r0 < sq ? max(0, min(last_key / C::BN + 1, je) - jb) : 0;
   }
   const int nb_max = max(nb[0], nb[1]);
   if (nb_max == 0) {
@@ -131,13 +142,13 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // (o = 0, lse = -inf). The condition is uniform over the CTA, so every
     // thread leaves before any barrier.
     if (a.n_split > 1) {
-      if (threadIdx.x < 256) {
-        const int row = qblk * 256 + (int)threadIdx.x;
+      if ((int)threadIdx.x < C::kRows) {
+        const int row = qblk * C::kRows + (int)threadIdx.x;
         if (row < Nq) a.lse_part[((size_t)blockIdx.z * a.BH + bh) * Nq + row] = -INFINITY;
       }
     } else if (VARLEN) {
-      const int r0 = qblk * 256;
-      zero_rows<D>(a, bh, r0, min(256, Nq - r0), (int)threadIdx.x, (int)blockDim.x);
+      const int r0 = qblk * C::kRows;
+      zero_rows<D>(a, bh, r0, min(C::kRows, Nq - r0), (int)threadIdx.x, (int)blockDim.x);
     }
     return;
   }
@@ -162,8 +173,8 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
-    tmem_alloc(&bars.tmem_base, 512);
+  if (warp == C::kWarpMma) {
+    tmem_alloc(&bars.tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == 8) {
+  if (warp == C::kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     // Q tile 0, then K and V of each key block, with Q tile 1 between K and
     // V of the first block (the first S needs Q tile 0 and K only). The whole
@@ -182,7 +193,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         for (int pn = 0; pn < C::kPanels; ++pn)
           tma_load_3d(smem + C::kOffQ + t * C::kQSlotBytes + pn * C::kPanelBytes, &a.tm_q, &bars.q_full[t],
                       pn * (128 / C::kElem),
-                      qblk * 256 + t * 128, bh);
+                      qblk * C::kRows + t * 128, bh);
       }
       __syncwarp();
     };
@@ -206,7 +217,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       }
       __syncwarp();
       nk_issued = j + 1;
-      if (j == 0) {
+      if (C::kTiles == 2 && j == 0) {
         load_q(1);
         q1_issued = true;
       }
@@ -227,7 +238,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
     for (int i = max(0, nv_issued - C::kVStages); i < nv_issued; ++i)
       mbar_wait_drain(&bars.v_full[i % C::kVStages], (i / C::kVStages) & 1);
-  } else if (warp == 9) {
+  } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp follows the schedule, so it stays converged and its
     // operands warp-uniform; one elected lane issues each group of tcgen05
@@ -262,12 +273,12 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         tc_fence_after();
         if (elect_one() && nb[0] > 0) issue_s(0, 0);
         __syncwarp();
-        ok = warp_wait(&bars.q_full[1], 0, abort_flag);
+        if (C::kTiles == 2) ok = warp_wait(&bars.q_full[1], 0, abort_flag);
       }
       if (ok) {
         tc_fence_after();
         if (elect_one()) {
-          if (nb[1] > 0) issue_s(1, 0);
+          if (C::kTiles == 2 && nb[1] > 0) issue_s(1, 0);
           mma_commit(&bars.k_empty[0]);
         }
         __syncwarp();
@@ -289,7 +300,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
         ok = warp_wait3(&bars.v_full[s], ph, j < nb[0] ? &bars.p_full[0] : &bars.v_full[s], j < nb[0] ? (j & 1) : ph,
                         k_next ? &bars.k_full[sn] : &bars.v_full[s], k_next ? (jn / C::kKStages) & 1 : ph, abort_flag);
         if (!ok) break;
-        for (int t = 0; t < 2 && ok; ++t) {
+        for (int t = 0; t < C::kTiles && ok; ++t) {
           if (j < nb[t]) {
             if (t == 1 && !(ok = warp_wait(&bars.p_full[t], j & 1, abort_flag))) break;
             tc_fence_after();
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
     // ------------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
-    const int r0 = qblk * 256 + t * 128;
+    const int r0 = qblk * C::kRows + t * 128;
     const int row = r0 + r;
     const int nbt = nb[t];
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
       named_bar_sync(1 + t, 128);
       if (r == 0 && !*abort_flag) {
         for (int pn = 0; pn < C::kOPanels; ++pn)
-          tma_store_3d(&a.tm_o, stage + pn * C::kPanelBytes, pn * 64, qblk * 256 + t * 128, bh);
+          tma_store_3d(&a.tm_o, stage + pn * C::kPanelBytes, pn * 64, qblk * C::kRows + t * 128, bh);
         bulk_commit();
         bulk_wait_read0();  // the staging tile has been read; the writes finish on their own
       }
@@ -536,7 +547,7 @@ __global__ void __launch_bounds__(320, 1) fa_fwd_kernel(const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == C::kWarpMma) tmem_dealloc(tmem, C::kTmemCols);
   if (threadIdx.x == 0 && bars.abort) atomicOr(a.status, 1u);
 }
 
@@ -582,17 +593,19 @@ template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   auto kern = a.seqlens_q || a.seqlens_k ? fa_fwd_kernel<D, CAUSAL, true> : fa_fwd_kernel<D, CAUSAL, false>;
   if (a.drop_p256 > 0) kern = fa_fwd_kernel<D, CAUSAL, false, false, true>;  // dropout: no lengths, no key ranges
-  int smem = FwdCfg<D>::kSmemBytes;
+  int smem = FwdCfg<D>::kSmemBytes, threads = FwdCfg<D>::kThreads, rows = FwdCfg<D>::kRows;
   if constexpr (D == 128) {
     if (a.fp8) {  // 8-bit inputs: no lengths, no key ranges
       kern = fa_fwd_kernel<D, CAUSAL, false, true>;
       smem = FwdCfg<D, true>::kSmemBytes;
+      threads = FwdCfg<D, true>::kThreads;
+      rows = FwdCfg<D, true>::kRows;
     }
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + 255) / 256), (unsigned)a.n_split);
-  kern<<<grid, 320, smem, stream>>>(a);
+  const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + rows - 1) / rows), (unsigned)a.n_split);
+  kern<<<grid, threads, smem, stream>>>(a);
   if (a.n_split > 1) {
     const long long rows = (long long)a.BH * a.Nq;
     fa_fwd_merge_kernel<D><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(a);
@@ -605,7 +618,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdArgs& args, int num_sms, cudaStream_t stream) {
   FwdArgs a = args;
   // a CTA's fixed cost (loads before the first product, epilogue) is about two key blocks of work
-  a.head_group = pick_head_group(a.BH, (a.Nq + 255) / 256, a.causal != 0, num_sms, 2.0);
+  const int rows = fwd_rows_per_cta(a.d), slots = num_sms * fwd_ctas_per_sm(a.d);
+  a.head_group = pick_head_group(a.BH, (a.Nq + rows - 1) / rows, a.causal != 0, slots, 2.0);
   if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
   return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
 }

@@ -91,6 +91,11 @@ __device__ inline bool seq_lens(const int* lq, const int* lk, int b, int Nq, int
   return bad;
 }
 
+// Forward CTA shape for head dimension d: query rows per CTA and CTAs that
+// share an SM (d = 64: one 128-row tile, two CTAs per SM; else two tiles, one).
+inline int fwd_rows_per_cta(int d) { return d == 64 ? 128 : 256; }
+inline int fwd_ctas_per_sm(int d) { return d == 64 ? 2 : 1; }
+
 // Heads per CTA scheduling group for a (BH x nblk) grid whose causal CTAs
 // cost nblk - blk units of work plus 'overhead' units each (schedule.cu).
 int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead);
@@ -98,10 +103,11 @@ int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead)
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
 // Key ranges worth splitting a forward into (1 = no split, when the query
-// blocks alone fill the SMs): the fewest whose CTAs fill their waves of one CTA
-// per SM to 90%, each range at least two 128-key blocks, at most kMaxKeySplits.
+// blocks alone fill the SMs): the fewest whose CTAs (rows_per_cta query rows
+// each) fill their waves of num_slots CTAs (SMs x CTAs per SM) to 90%, each
+// range at least two 128-key blocks, at most kMaxKeySplits.
 constexpr int kMaxKeySplits = 32;
-int pick_key_splits(int BH, int Nq, int Nk, int num_sms);
+int pick_key_splits(int BH, int Nq, int Nk, int num_slots, int rows_per_cta);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace fa

@@ -92,11 +92,11 @@ int pick_head_group(int BH, int nblk, bool causal, int num_sms, double overhead)
   return chosen;
 }
 
-int pick_key_splits(int BH, int Nq, int Nk, int num_sms) {
-  const long long ctas = (long long)BH * ((Nq + 255) / 256);  // CTAs without a split
+int pick_key_splits(int BH, int Nq, int Nk, int num_sms, int rows_per_cta) {
+  const long long ctas = (long long)BH * ((Nq + rows_per_cta - 1) / rows_per_cta);  // CTAs without a split
   const int nkv = (Nk + 127) / 128;
   if (num_sms <= 0 || ctas >= num_sms || nkv < 4) return 1;
-  // The fewest ranges whose CTAs fill their waves of one CTA per SM to 90%
+  // The fewest ranges whose CTAs fill their waves of num_sms CTA slots to 90%
   // (a short last wave would double the time of a bandwidth-bound call), else
   // the best filling; each range at least two key blocks.
   const int cap = (int)std::min<long long>(kMaxKeySplits, nkv / 2);

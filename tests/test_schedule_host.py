@@ -96,10 +96,10 @@ def test_cached_answers_are_stable(picker):
 
 SPLIT_DRIVER = r"""
 #include <cstdio>
-namespace fa { int pick_key_splits(int BH, int Nq, int Nk, int num_sms); }
+namespace fa { int pick_key_splits(int BH, int Nq, int Nk, int num_slots, int rows_per_cta); }
 int main() {
   int BH, Nq, Nk, sms;
-  while (scanf("%d %d %d %d", &BH, &Nq, &Nk, &sms) == 4) printf("%d\n", fa::pick_key_splits(BH, Nq, Nk, sms));
+  while (scanf("%d %d %d %d", &BH, &Nq, &Nk, &sms) == 4) printf("%d\n", fa::pick_key_splits(BH, Nq, Nk, sms, 256));
   return 0;
 }
 """
