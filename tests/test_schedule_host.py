@@ -98,8 +98,9 @@ SPLIT_DRIVER = r"""
 #include <cstdio>
 namespace fa { int pick_key_splits(int BH, int Nq, int Nk, int num_slots, int rows_per_cta); }
 int main() {
-  int BH, Nq, Nk, sms;
-  while (scanf("%d %d %d %d", &BH, &Nq, &Nk, &sms) == 4) printf("%d\n", fa::pick_key_splits(BH, Nq, Nk, sms, 256));
+  int BH, Nq, Nk, slots, rows;
+  while (scanf("%d %d %d %d %d", &BH, &Nq, &Nk, &slots, &rows) == 5)
+    printf("%d\n", fa::pick_key_splits(BH, Nq, Nk, slots, rows));
   return 0;
 }
 """
@@ -116,8 +117,8 @@ def splitter(tmp_path_factory):
     subprocess.check_call([gxx, "-O2", "-std=c++17", "-x", "c++", os.path.join(CSRC, "schedule.cu"), "-x", "c++",
                            str(d / "driver.cpp"), "-I", CSRC, "-I", "/usr/local/cuda/include", "-o", str(exe)])
 
-    def pick(cases):
-        inp = "".join(f"{bh} {nq} {nk} {sms}\n" for bh, nq, nk, sms in cases)
+    def pick(cases, rows=256):
+        inp = "".join(f"{bh} {nq} {nk} {sms} {rows}\n" for bh, nq, nk, sms in cases)
         return [int(x) for x in subprocess.run([str(exe)], input=inp, capture_output=True, text=True,
                                                check=True).stdout.split()]
     return pick
@@ -138,3 +139,19 @@ def test_key_splits(splitter):
         better = [m for m in range(1, min(32, nkv // 2) + 1) if fill(m) >= 0.9]
         assert n == (better[0] if better else max(range(1, min(32, nkv // 2) + 1), key=lambda m: (fill(m), -m)))
     assert got[3] == 9  # 32 heads x 1 query block: 288 CTAs = 95% of two waves
+
+
+def test_key_splits_two_ctas_per_sm(splitter):
+    """At d = 64 a CTA covers 128 query rows and two share an SM: the waves hold 2 x SMs CTAs."""
+    cases = [(32, 1, 65536, 304), (64, 256, 8192, 304), (2, 130, 16384, 304), (128, 300, 4096, 304)]
+    got = splitter(cases, rows=128)
+    assert got[3] == 1  # 128 heads x 3 query blocks = 384 CTAs: more than the 304 slots
+    for (bh, nq, nk, slots), n in zip(cases, got):
+        ctas = bh * ((nq + 127) // 128)
+        nkv = (nk + 127) // 128
+        fill = lambda m: ctas * m / (-(-ctas * m // slots) * slots)  # noqa: E731
+        if ctas >= slots:
+            assert n == 1
+            continue
+        better = [m for m in range(1, min(32, nkv // 2) + 1) if fill(m) >= 0.9]
+        assert n == (better[0] if better else max(range(1, min(32, nkv // 2) + 1), key=lambda m: (fill(m), -m)))
