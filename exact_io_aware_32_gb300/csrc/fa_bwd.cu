@@ -31,6 +31,11 @@
 // next product. Each S or dP tile is released to the MMA warp as soon as the
 // warpgroups hold it in registers, so the next tile's product overlaps their
 // elementwise work.
+//
+// Template flags add per-sequence lengths (padding masks: each tile reads its
+// sequence's lengths) and dropout (the forward's Philox mask made again from
+// the seed, applied to P^T for dV and to dP in dS) without changing the plain
+// kernels.
 #include <cuda_bf16.h>
 
 #include <algorithm>

@@ -1,7 +1,8 @@
 // Forward pass of exact attention on sm_103a.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and streams the
-// head's key/value blocks (128 rows each) past them, as in the blocked loop of
+// One CTA owns two 128-row query tiles of one (batch, head) (one tile at
+// d = 64, where two CTAs share an SM) and streams the head's key/value blocks
+// (128 rows each) past them, as in the blocked loop of
 // "FlashAttention and GPU Memory", chapter 07 (each SM takes one block of Q at
 // a time; blocks of K and V fly in; only O is written back). Per key block and
 // query tile:
@@ -13,11 +14,17 @@
 //   O += P V                  tcgen05.mma, P read back from TMEM as bf16
 // and at the end O / l and the row logsumexp are written.
 //
-// Warp roles (320 threads): warps 0-3 and 4-7 are the softmax/epilogue
-// warpgroups of query tiles 0 and 1, warp 8 issues TMA loads, warp 9 issues
-// the MMAs and owns the TMEM allocation. The two tiles alternate on the tensor
-// core so that one tile's softmax overlaps the other tile's products (the
-// staggering the pages describe for the third version, chapter 11).
+// Warp roles (320 threads with two tiles): warps 0-3 and 4-7 are the
+// softmax/epilogue warpgroups of query tiles 0 and 1, warp 8 issues TMA loads,
+// warp 9 issues the MMAs and owns the TMEM allocation (with one tile: warps
+// 0-3, 4 and 5). The tiles alternate on the tensor core, within a CTA or
+// between the two CTAs of an SM, so that one tile's softmax overlaps the other
+// tile's products (the staggering the pages describe for the third version,
+// chapter 11).
+//
+// Template flags add the other variants without changing this one: per-
+// sequence lengths (padding masks), E4M3 inputs with 8-bit products, and
+// dropout of P with a Philox mask.
 //
 // The running maximum used as the exponent reference is only moved when the
 // true row maximum exceeds it by more than 2^8; O and l are always scaled
