@@ -5,7 +5,8 @@ of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
 ``fa_fwd_kv_workspace_bytes``, ``fa_fwd_fp8``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
 ``fa_bwd_kv_workspace_bytes``,
 ``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
-torch CUDA tensors or raw device addresses (ints). ``forward``,
+torch CUDA tensors or raw device addresses (ints). ``attention`` is a
+differentiable torch.autograd.Function over the forward and backward calls; ``forward``,
 ``forward_kv``, ``forward_fp8``, ``forward_dropout``, ``backward``, ``backward_kv`` and
 ``backward_dropout`` are conveniences that
 allocate the outputs with torch.
@@ -198,10 +199,61 @@ def _shape(q):
     return tuple(int(s) for s in q.shape)
 
 
+def _bf16(*ts):
+    """The 16-bit entry points read raw device memory: bf16, contiguous, on the GPU."""
+    import torch
+
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("expected contiguous bf16 CUDA tensors")
+
+
+_attention_fn = None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, dropout_p256: int = 0, seed: int = 0,
+              offset: int = 0):
+    """Differentiable attention o = softmax(scale q k^T [causal]) v (with dropout of probability
+    dropout_p256 / 256 after the softmax if given) for q, k, v of shape [B, H, N, d], bf16: a
+    torch.autograd.Function whose forward runs fa_fwd (fa_fwd_dropout) and whose backward runs fa_bwd
+    (fa_bwd_dropout, the same mask made again from seed and offset)."""
+    global _attention_fn
+    if _attention_fn is None:
+        import torch
+
+        class _Attention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale, p256, seed, offset):
+                if p256:
+                    o, lse = forward_dropout(q, k, v, p256, seed, offset, causal=causal, scale=scale)
+                else:
+                    o, lse = forward(q, k, v, causal=causal, scale=scale)
+                ctx.save_for_backward(q, k, v, o, lse)
+                ctx.args = (causal, scale, p256, seed, offset)
+                return o
+
+            @staticmethod
+            def backward(ctx, dO):
+                q, k, v, o, lse = ctx.saved_tensors
+                causal, scale, p256, seed, offset = ctx.args
+                dO = dO.to(torch.bfloat16).contiguous()
+                if p256:
+                    dq, dk, dv = backward_dropout(q, k, v, o, lse, dO, p256, seed, offset, causal=causal, scale=scale)
+                else:
+                    dq, dk, dv = backward(q, k, v, o, lse, dO, causal=causal, scale=scale)
+                return dq, dk, dv, None, None, None, None, None
+
+        _attention_fn = _Attention
+    _bf16(q, k, v)
+    scale = 1.0 / math.sqrt(int(q.shape[-1])) if scale is None else scale
+    return _attention_fn.apply(q, k, v, bool(causal), float(scale), int(dropout_p256), int(seed), int(offset))
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
     """Allocate o (bf16) and lse (fp32) with torch and run fa_fwd. Returns (o, lse)."""
     import torch
 
+    _bf16(q, k, v)
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
@@ -236,6 +288,7 @@ def forward_dropout(q, k, v, p256: int, seed: int, offset: int = 0, causal: bool
     """Forward with dropout probability p256 / 256 (Philox mask of seed, offset). Returns (o, lse)."""
     import torch
 
+    _bf16(q, k, v)
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
@@ -251,6 +304,7 @@ def backward_dropout(q, k, v, o, lse, dO, p256: int, seed: int, offset: int = 0,
     """Backward of forward_dropout with the same (p256, seed, offset). Returns (dq, dk, dv)."""
     import torch
 
+    _bf16(q, k, v, o, dO)
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -270,6 +324,7 @@ def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, split:
     ``seqlens_k`` are optional int32 [B] device tensors (padding masks). Returns (o, lse)."""
     import torch
 
+    _bf16(q, k, v)
     B, H, Nq, d = _shape(q)
     Nk = int(k.shape[2])
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -288,6 +343,7 @@ def backward(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = No
     """Allocate dq, dk, dv (and the workspace if none is given) and run fa_bwd."""
     import torch
 
+    _bf16(q, k, v, o, dO)
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -307,6 +363,7 @@ def backward_kv(q, k, v, o, lse, dO, causal: bool = False, scale: float | None =
     (``seqlens_q`` / ``seqlens_k`` as in forward_kv)."""
     import torch
 
+    _bf16(q, k, v, o, dO)
     B, H, Nq, d = _shape(q)
     Nk = int(k.shape[2])
     scale = 1.0 / math.sqrt(d) if scale is None else scale
