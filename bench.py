@@ -33,6 +33,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -208,18 +209,27 @@ def cpu_baseline(w, causal: bool, budget_s: float = 12.0) -> dict:
 
 
 # ---------------------------------------------------------------------- GPU arm
+def code_sha(source: str) -> str:
+    """sha256 of a kernel source with its comments and blank lines removed: a comment edit leaves it
+    unchanged, any change to the code changes it."""
+    with open(os.path.join(ROOT, "exact_io_aware_32_gb300", "csrc", source)) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def kernel_traffic(source: str, kernel: str):
-    """DRAM bytes per call from a committed ncu capture, or None if the kernel source changed since."""
+    """DRAM bytes per call from a committed ncu capture, or None if the kernel code changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             entries = json.load(f)
     except (OSError, ValueError):
         return None
-    with open(os.path.join(ROOT, "exact_io_aware_32_gb300", "csrc", source), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
     e = entries.get(kernel)
-    if not e or e.get("source_sha256") != sha:
+    if not e or e.get("code_sha256") != code_sha(source):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -1,7 +1,7 @@
 // Backward pass of exact attention on sm_103a.
 //
 // The pages keep only O and the per-row statistics from the forward pass and
-// rebuild S and P block by block from Q, K and V ("FlashAttention and GPU
+// compute the score and probability tiles again from Q, K and V ("FlashAttention and GPU
 // Memory", chapter 09). With lse_i the row logsumexp, for a block of keys j
 // and a block of queries i:
 //   S = Q_i K_j^T,  P = exp(scale S - lse_i),  dP = dO_i V_j^T,

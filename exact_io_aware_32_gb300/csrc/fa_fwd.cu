@@ -3,9 +3,9 @@
 // One CTA owns two 128-row query tiles of one (batch, head) (one tile at
 // d = 64, where two CTAs share an SM) and streams the head's key/value blocks
 // (128 rows each) past them, as in the blocked loop of
-// "FlashAttention and GPU Memory", chapter 07 (each SM takes one block of Q at
-// a time; blocks of K and V fly in; only O is written back). Per key block and
-// query tile:
+// "FlashAttention and GPU Memory", chapter 07 (a query block stays on the SM
+// while the key and value blocks stream through; of all the results, only O
+// goes back to device memory). Per key block and query tile:
 //   S = Q K^T                 tcgen05.mma, bf16 operands from shared memory,
 //                             fp32 accumulator in tensor memory (TMEM)
 //   m, l, P                   running row max / sum of exponentials (chapter

@@ -8,9 +8,9 @@ Conventions (the pages state none, so these are stated here):
 * Compulsory bytes of the tiled method: forward reads q, k, v and writes o
   (bf16) and lse (fp32); backward reads q, k, v, o, dO (bf16) and lse (fp32),
   writes dq, dk, dv (bf16) and writes and reads D (fp32).
-* The "standard way" (S = QK^T written to HBM, read back for P = softmax(S),
+* The unfused computation (S = QK^T written to HBM, read back for P = softmax(S),
   P written and read back for O = PV) moves q, k, v, o once each plus S and P
-  out and back once each ("FlashAttention and GPU Memory", chapters 03-04).
+  to device memory and read back once each ("FlashAttention and GPU Memory", chapters 03-04).
 * The page's laboratory counts the second version's loop order as: each block
   of Q read once, all of K and V read once per block of Q, O written once,
   with no help from L2 (chapter 14).

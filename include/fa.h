@@ -6,8 +6,8 @@
  * slices of that head,
  *     O = softmax(scale * q k^T [+ causal mask]) v
  * exactly, not an approximation: the pages this follows state that the tiled
- * method returns softmax(QK^T)V "with no approximation" and differs from a
- * whole-matrix computation only by floating-point rounding
+ * method returns softmax(QK^T)V itself, differing from a whole-matrix
+ * computation only by floating-point rounding
  * ("FlashAttention does more arithmetic to move less data", section
  * "FlashAttention never writes the full score table to HBM";
  * "FlashAttention and GPU Memory", chapters 01, 08 and 12). The N x N score
@@ -17,7 +17,7 @@
  * The forward pass also returns one number per row, the natural-log
  * logsumexp of the scaled, masked scores, which folds the running maximum m
  * and running sum l that the method keeps per row (chapter 08, "A softmax with
- * a running tally"; chapter 09 keeps "two numbers per row"). The backward
+ * a running tally"; chapter 09 keeps those two values for each row). The backward
  * pass rebuilds score tiles from q, k, v and that logsumexp instead of
  * reading a stored probability matrix (chapter 09, "Backward: recomputing
  * beats reading").
@@ -229,7 +229,7 @@ FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const voi
 /*
  * Forward and backward with dropout of P after the softmax ("FlashAttention
  * and GPU Memory": chapter 07 fuses dropout into the one kernel; chapter 09's
- * backward keeps only the generator's state and makes the mask again).
+ * backward stores no mask: it regenerates it from the generator's state).
  *   p256     dropout probability p256 / 256, 0 .. 255 (FA_ERR_INVALID_ARG
  *            otherwise; 0 is the plain pass); kept elements are scaled by
  *            256 / (256 - p256)

@@ -6,7 +6,7 @@
  *
  * It computes the definition of attention written out, not a tiled
  * algorithm. The pages state that the IO-aware method returns exactly
- * softmax(Q K^T) V "with no approximation" ("FlashAttention does more
+ * softmax(Q K^T) V, without approximating it ("FlashAttention does more
  * arithmetic to move less data", section "FlashAttention never writes the
  * full score table to HBM"; "FlashAttention and GPU Memory", chapter 01 and
  * chapter 12), so the definition is the oracle.
@@ -42,7 +42,8 @@
  *   lse_i = M_i + ln l_i              (the natural-log logsumexp of the row)
  *
  * Backward, by the chain rule on the same definition (the pages only say that
- * S and P are rebuilt from Q, K, V and the saved row statistics, chapter 09):
+ * the backward recomputes the score and probability tiles from Q, K, V and
+ * the per-row values the forward kept, chapter 09):
  *   dP_ij = dO_i . v_j
  *   D_i   = sum_{j in A(i)} P_ij dP_ij   (summed explicitly, not as dO_i . o_i)
  *   dS_ij = P_ij (dP_ij - D_i)
@@ -411,8 +412,8 @@ int oracle_fwd_fp8(const unsigned char* q8, const unsigned char* k8, const unsig
 
 /*
  * Dropout ("FlashAttention and GPU Memory", chapter 07: dropout is one of
- * the steps fused into the single kernel; chapter 09: the backward keeps only
- * the random-number generator's state and makes the mask again). The pages
+ * the steps fused into the single kernel; chapter 09: the backward stores no
+ * mask, only what is needed to regenerate it). The pages
  * fix neither the generator nor the mask's layout; the readings taken here:
  *
  *   - the generator is Philox4x32-10 (Salmon, Moraes, Dror and Shaw,

@@ -9,8 +9,8 @@ Three independent views of the same definition live here:
 * ``fwd`` / ``bwd`` call the streaming C implementation in ``fa_oracle.c``
   (the definition, row by row, fp64, OpenMP over rows and keys);
 * ``materialised_fwd`` / ``materialised_bwd`` build the full N x N score
-  matrix S and probability matrix P with numpy, in the order the pages call
-  "the standard way" ("FlashAttention and GPU Memory", chapter 04: S = QK^T,
+  matrix S and probability matrix P with numpy, in the order the pages give
+  for the usual, unfused computation ("FlashAttention and GPU Memory", chapter 04: S = QK^T,
   then P = softmax(S), then O = PV), for tiny inputs only;
 * ``online_softmax`` carries the running maximum m and running sum l block by
   block, with the update rule of chapter 08 of the same page

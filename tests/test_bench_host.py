@@ -35,6 +35,19 @@ def test_decode_and_fp8_workload_names():
     assert bench.fp8_spec("d128_n4096_causal") is None and bench.decode_spec("fp8_4_32_4096_causal") is None
 
 
+def test_code_sha_ignores_comments_only(tmp_path, monkeypatch):
+    """The traffic figures stay valid across comment edits of a kernel source and not across code edits."""
+    csrc = tmp_path / "exact_io_aware_32_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "k.cu").write_text("// head\nint f(int x) {  // note\n  return x + 1; /* a\n b */\n}\n")
+    a = bench.code_sha("k.cu")
+    (csrc / "k.cu").write_text("/* other words */\nint f(int x) {\n\n  return x + 1;\n}  // tail\n")
+    assert bench.code_sha("k.cu") == a
+    (csrc / "k.cu").write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.code_sha("k.cu") != a
+
+
 def test_aggregate_uses_slowest_rank():
     v, t = bench.aggregate([1.0, 2.0, 1.5], [10.0, 10.0, 10.0])
     assert t == 2.0 and v == 15.0
