@@ -465,6 +465,20 @@ int oracle_dropout_byte(unsigned long long seed, unsigned int offset, int bh, in
   return (int)((out[i & 3] >> (8 * (j & 3))) & 0xFFu);
 }
 
+/* The keep decisions of every element of heads 0 .. BH - 1 with N queries and
+ * N keys: keep[(bh * N + i) * N + j] = 1 iff byte(bh, i, j) >= p256. */
+int oracle_dropout_keep(unsigned long long seed, unsigned int offset, int BH, int N, int p256, unsigned char* keep,
+                        int nthreads) {
+  if (BH < 1 || N < 1 || p256 < 0 || p256 > 255 || !keep) return 1;
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long long r = 0; r < (long long)BH * N; ++r) {
+    const int bh = (int)(r / N), i = (int)(r % N);
+    for (int j = 0; j < N; ++j) keep[r * N + j] = oracle_dropout_byte(seed, offset, bh, i, j) >= p256;
+  }
+  return 0;
+}
+
 /* Z_ij: 0 if the element is dropped, else 256 / (256 - p256). */
 static double drop_factor(unsigned long long seed, unsigned int offset, int bh, int i, int j, int p256) {
   return oracle_dropout_byte(seed, offset, bh, i, j) >= p256 ? 256.0 / (256.0 - p256) : 0.0;

@@ -97,6 +97,8 @@ def load(path: str | None = None):
         lib.oracle_bwd_drop.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int, c_double, c_int, c_int,
                                         c_u64, c_u32, c_int]
         lib.oracle_bwd_drop.restype = c_int
+        lib.oracle_dropout_keep.argtypes = [c_u64, c_u32, c_int, c_int, c_int, u8p, c_int]
+        lib.oracle_dropout_keep.restype = c_int
         lib.oracle_max_threads.argtypes = [c_int]
         lib.oracle_max_threads.restype = c_int
         if path is None:
@@ -296,6 +298,17 @@ def philox4x32_10(ctr, key, lib=None):
 def dropout_byte(seed: int, offset: int, bh: int, i: int, j: int, lib=None) -> int:
     """The random byte of element (query i, key j) of head bh; kept iff byte >= p256."""
     return int((lib or load()).oracle_dropout_byte(int(seed), int(offset), int(bh), int(i), int(j)))
+
+
+def dropout_keep(seed: int, offset: int, BH: int, N: int, p256: int, nthreads: int = 0, lib=None) -> np.ndarray:
+    """Keep decisions of heads 0 .. BH - 1 (N queries x N keys each): bool [BH, N, N],
+    element (bh, i, j) = dropout_byte(seed, offset, bh, i, j) >= p256."""
+    keep = np.zeros((BH, N, N), dtype=np.uint8)
+    rc = (lib or load()).oracle_dropout_keep(int(seed), int(offset), int(BH), int(N), int(p256),
+                                             keep.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_dropout_keep failed")
+    return keep.astype(bool)
 
 
 def fwd_drop(q, k, v, scale: float, causal: bool, p256: int, seed: int, offset: int = 0, rows=None,

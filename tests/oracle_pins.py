@@ -505,6 +505,16 @@ def pin_dropout_keep_rate(lib=None):
     assert chi2 < 255 + 6 * math.sqrt(2 * 255)  # 255 degrees of freedom
 
 
+def pin_dropout_keep_mask(lib=None):
+    """The whole-array keep mask equals the Philox structure above, element by element (odd N, so that
+    rows and keys straddle the 4 x 4 blocks of one generator call)."""
+    BH, N, p256, seed, off = 3, 37, 101, 0x0123456789AB, 17
+    keep = orc.dropout_keep(seed, off, BH, N, p256, lib=lib)
+    want = np.array([[[_drop_byte(seed, off, h, i, j) >= p256 for j in range(N)] for i in range(N)]
+                     for h in range(BH)])
+    assert keep.shape == (BH, N, N) and np.array_equal(keep, want)
+
+
 def pin_dropout_brute_force(lib=None):
     """A tiny dropout forward with numpy and the mask from the Philox structure above:
     o_i = sum_j softmax_j * [byte_ij >= p256] * 256 / (256 - p256) * v_j; lse as without dropout."""
@@ -570,6 +580,7 @@ ALL_PINS = [
     pin_philox,
     pin_dropout_zero_is_plain,
     pin_dropout_keep_rate,
+    pin_dropout_keep_mask,
     pin_dropout_brute_force,
     pin_dropout_gradients,
 ]
