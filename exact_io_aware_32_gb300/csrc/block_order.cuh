@@ -20,9 +20,4 @@ __device__ __forceinline__ void grouped_index(int linear, int BH, int nblk, int 
   bh = g * group + (idx - blk * gsize);
 }
 
-// The same for the CTA's own linear index in a (BH, nblk) grid.
-__device__ __forceinline__ void grouped_block(int BH, int nblk, int group, int& bh, int& blk) {
-  grouped_index((int)(blockIdx.x + blockIdx.y * gridDim.x), BH, nblk, group, bh, blk);
-}
-
 }  // namespace fa

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -33,6 +34,9 @@ DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int fail_launch() { return FA_ERR_LAUNCH; }
+
+// Fault armed by fa_test_arm_fault for the next forward launch (0: none).
+std::atomic<int> g_test_fault{0};
 
 // Per-device facts, looked up once per device with that device current.
 int device_info(DeviceInfo** out) {
@@ -81,8 +85,8 @@ int check_shape(int B, int H, int N, int d, float scale) {
 
 // Tensor map over a contiguous [BH][N][d] tensor, boxes of box_x columns by
 // box_rows rows of one head, 128-byte swizzle (box_x * elem == 128 bytes).
-bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem, int BH, int N, int d,
-               int box_x, int box_rows) {
+bool encode_3d_uncached(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem, int BH, int N, int d,
+                        int box_x, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * elem, (cuuint64_t)N * d * elem};
   cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)box_rows, 1};
@@ -91,6 +95,64 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int 
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Encoded tensor maps, keyed by everything the encoding depends on: a map
+// holds only the base address and the geometry, so an entry stays valid for
+// any later buffer at that address with that shape and type (a freed and
+// reused address with another shape is simply another key). A small set-
+// associative table: 64 sets of 4 ways, least recently used way replaced.
+struct MapKey {
+  const void* base;
+  int dev, dtype, elem, BH, N, d, box_x, box_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && dev == o.dev && dtype == o.dtype && elem == o.elem && BH == o.BH && N == o.N &&
+           d == o.d && box_x == o.box_x && box_rows == o.box_rows;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  unsigned long long used;  // 0: empty
+};
+constexpr int kMapSets = 64, kMapWays = 4;
+MapEntry g_maps[kMapSets][kMapWays];
+unsigned long long g_map_clock = 0;
+std::mutex g_map_mu;
+
+int map_set(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.base) >> 8;
+  h ^= (uint64_t)(unsigned)k.N * 0x9E3779B97F4A7C15ull;
+  h ^= (uint64_t)(unsigned)k.BH * 0xC2B2AE3D27D4EB4Full;
+  h ^= (uint64_t)(unsigned)(k.d + 131 * k.box_x + 17 * k.dtype + 7 * k.dev);
+  h ^= h >> 29;
+  return (int)(h % kMapSets);
+}
+
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem, int BH, int N, int d,
+               int box_x, int box_rows) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const MapKey key{base, dev, (int)dtype, elem, BH, N, d, box_x, box_rows};
+  MapEntry* set = g_maps[map_set(key)];
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int w = 0; w < kMapWays; ++w)
+      if (set[w].used && set[w].key == key) {
+        set[w].used = ++g_map_clock;
+        *m = set[w].map;
+        return true;
+      }
+  }
+  if (!encode_3d_uncached(m, base, dtype, elem, BH, N, d, box_x, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  int victim = 0;
+  for (int w = 1; w < kMapWays; ++w)
+    if (set[w].used < set[victim].used) victim = w;
+  set[victim].key = key;
+  set[victim].map = *m;
+  set[victim].used = ++g_map_clock;
+  return true;
 }
 
 constexpr double kLog2e = 1.4426950408889634074;
@@ -218,6 +280,7 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
     a.o_part = static_cast<float*>(workspace);
     a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * d * sizeof(float)));
   }
+  a.test_fault = g_test_fault.exchange(0);
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -258,6 +321,7 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, flo
   a.causal = causal ? 1 : 0;
   a.split_blocks = (N + 127) / 128;
   a.n_split = 1;
+  a.test_fault = g_test_fault.exchange(0);
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -293,6 +357,7 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
   fa::philox::round_keys(seed, a.drop_rk);
   a.split_blocks = (N + 127) / 128;
   a.n_split = 1;
+  a.test_fault = g_test_fault.exchange(0);
   return fa::launch_fwd(a, di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -338,6 +403,12 @@ const char* fa_status_string(int status) {
     case FA_ERR_TIMEOUT: return "a kernel wait timed out";
     default: return "unknown status";
   }
+}
+
+int fa_test_arm_fault(int kind) {
+  if (kind < 0 || kind > 1) return FA_ERR_INVALID_ARG;
+  g_test_fault.store(kind);
+  return FA_OK;
 }
 
 int fa_device_status(int reset) {

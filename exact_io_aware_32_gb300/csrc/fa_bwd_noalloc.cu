@@ -31,14 +31,29 @@ std::mutex g_setup_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up on the
-// first call for that device. Returns FA_OK or FA_ERR_LAUNCH.
+// first call for that device. Returns FA_OK, FA_ERR_UNSUPPORTED (not an
+// sm_103 device: the library holds no code, hence no array, for it, and
+// fa_bwd reports the same) or FA_ERR_LAUNCH.
 int scratch_on_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // leave no error pending for the caller
+    return FA_ERR_LAUNCH;
+  }
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_ptr[dev]) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
+    if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) return FA_ERR_LAUNCH;
+    if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

@@ -123,9 +123,12 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Nq = a.Nq;  // rows of the q / o / lse arrays
+  // grid.x runs over (head, query block) pairs, so the number of query blocks
+  // is not bound by the 65535 limit of grid.y
+  const int nqblk = (Nq + C::kRows - 1) / C::kRows;
   int bh, blk;
-  grouped_block(a.BH, (int)gridDim.y, a.head_group, bh, blk);
-  const int qblk = CAUSAL ? (int)gridDim.y - 1 - blk : blk;  // heaviest first under the causal mask
+  grouped_index((int)blockIdx.x, a.BH, nqblk, a.head_group, bh, blk);
+  const int qblk = CAUSAL ? nqblk - 1 - blk : blk;  // heaviest first under the causal mask
   // this sequence's query rows sq and keys sk (all of them without padding masks)
   int sq = Nq, sk = a.Nk;
   if (VARLEN && seq_lens(a.seqlens_q, a.seqlens_k, bh / a.H, Nq, a.Nk, CAUSAL, sq, sk) && threadIdx.x == 0)
@@ -210,7 +213,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
       tma_prefetch_desc(&a.tm_v);
     }
     __syncwarp();
-    load_q(0);
+    // test hook: without the first Q tile, the MMA warp's first wait expires
+    const bool q0_issued = a.test_fault != 1;
+    if (q0_issued) load_q(0);
     bool q1_issued = false;
     int nk_issued = 0, nv_issued = 0;
     for (int j = 0; j < nb_max; ++j) {
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
       nv_issued = j + 1;
     }
     // Let every issued copy land before the CTA can exit.
-    mbar_wait_drain(&bars.q_full[0], 0);
+    if (q0_issued) mbar_wait_drain(&bars.q_full[0], 0);
     if (q1_issued) mbar_wait_drain(&bars.q_full[1], 0);
     for (int i = max(0, nk_issued - C::kKStages); i < nk_issued; ++i)
       mbar_wait_drain(&bars.k_full[i % C::kKStages], (i / C::kKStages) & 1);
@@ -611,7 +616,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)a.BH, (unsigned)((a.Nq + rows - 1) / rows), (unsigned)a.n_split);
+  const dim3 grid((unsigned)(a.BH * ((a.Nq + rows - 1) / rows)), 1u, (unsigned)a.n_split);
   kern<<<grid, threads, smem, stream>>>(a);
   if (a.n_split > 1) {
     const long long rows = (long long)a.BH * a.Nq;

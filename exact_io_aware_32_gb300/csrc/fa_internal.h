@@ -36,6 +36,10 @@ struct FwdArgs {
   int n_split, split_blocks;
   float* o_part;
   float* lse_part;
+  // Test hook (fa_test_arm_fault), 0 in normal use. 1: the load warp of every
+  // CTA withholds the first query tile's copy, so the MMA warp's bounded wait
+  // for it expires and the CTA takes its abort path.
+  int test_fault;
 };
 
 struct BwdArgs {

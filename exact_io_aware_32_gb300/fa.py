@@ -4,7 +4,7 @@ Argument marshalling only: every step of attention runs in the CUDA kernels
 of the library. The functions named like the C ABI (``fa_fwd``, ``fa_fwd_kv``,
 ``fa_fwd_kv_workspace_bytes``, ``fa_fwd_fp8``, ``fa_fwd_dropout``, ``fa_bwd_dropout``, ``fa_bwd``, ``fa_bwd_workspace_bytes``, ``fa_bwd_kv``,
 ``fa_bwd_kv_workspace_bytes``,
-``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``) take either
+``fa_status_string``, ``fa_device_status``, ``fa_bwd_noalloc``, ``fa_test_arm_fault``) take either
 torch CUDA tensors or raw device addresses (ints). ``attention`` is a
 differentiable torch.autograd.Function over the forward and backward calls; ``forward``,
 ``forward_kv``, ``forward_fp8``, ``forward_dropout``, ``backward``, ``backward_kv`` and
@@ -33,7 +33,7 @@ FA_ERR_TIMEOUT = 6
 
 EXPORTED = ("fa_fwd", "fa_fwd_kv", "fa_fwd_kv_workspace_bytes", "fa_fwd_fp8", "fa_fwd_dropout", "fa_bwd",
             "fa_bwd_workspace_bytes", "fa_bwd_kv", "fa_bwd_kv_workspace_bytes", "fa_bwd_dropout", "fa_status_string",
-            "fa_device_status", "fa_bwd_noalloc")
+            "fa_device_status", "fa_bwd_noalloc", "fa_test_arm_fault")
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +91,8 @@ def load(path: str | None = None):
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_device_status.argtypes = [c_int]
         lib.fa_device_status.restype = c_int
+        lib.fa_test_arm_fault.argtypes = [c_int]
+        lib.fa_test_arm_fault.restype = c_int
         if path is None:
             _lib = lib
         return lib
@@ -180,6 +182,12 @@ def fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B: int, H: int, Nq: int, Nk: int,
 
 def fa_device_status(reset: bool = True) -> int:
     return int(load().fa_device_status(int(bool(reset))))
+
+
+def fa_test_arm_fault(kind: int) -> int:
+    """Test hook: arm a one-shot fault for the next forward launch (1: withhold the first query
+    tile, so the kernels' bounded wait runs out and fa_device_status reports FA_ERR_TIMEOUT)."""
+    return int(load().fa_test_arm_fault(int(kind)))
 
 
 def _lens(x, B: int):

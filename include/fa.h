@@ -263,6 +263,23 @@ FA_API const char* fa_status_string(int status);
  */
 FA_API int fa_device_status(int reset);
 
+/*
+ * Test hook for the failure path; the pages have no counterpart to it. Arms a
+ * one-shot fault that the next forward launch (fa_fwd, fa_fwd_kv,
+ * fa_fwd_fp8 or fa_fwd_dropout, from any thread) consumes:
+ *   kind 1  every CTA's load warp withholds the copy of its first query
+ *           tile, so the MMA warp's bounded wait for it runs out after the
+ *           kernels' wait limit (one second). Each CTA then lets the copies
+ *           it issued land, frees its tensor memory, stores no output and sets
+ *           the device error word: fa_device_status returns FA_ERR_TIMEOUT.
+ *           The outputs of that call are left as they were; the stream and
+ *           the context remain usable.
+ *   kind 0  disarms a fault not yet consumed.
+ * Returns FA_OK, or FA_ERR_INVALID_ARG for another kind. Not for production
+ * use: it exists so that tests can drive the timeout path without a GPU fault.
+ */
+FA_API int fa_test_arm_fault(int kind);
+
 #ifdef __cplusplus
 }
 #endif

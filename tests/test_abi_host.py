@@ -207,3 +207,32 @@ def test_no_gpu_reports_launch_error(lib):
         pytest.skip("a GPU is present")
     st = fa.fa_fwd(A, A, A, A, A, 1, 1, 16, 64, 0.125, 0, stream=0)
     assert st == fa.FA_ERR_LAUNCH
+
+
+def test_noalloc_scratch_boundary_through_the_abi(lib):
+    """The largest shape fa_bwd_noalloc accepts is the one whose workspace need equals the built-in
+    scratch (B * H * N = 8,388,544 rows: align256(4 rows) + 256 = 32 MiB); one row more is rejected
+    with FA_ERR_WORKSPACE before anything is launched. Without a GPU the accepted shape then fails at
+    the device lookup (FA_ERR_LAUNCH), so no kernel is ever started with these fake addresses."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the accepted shape would launch on fake addresses")
+    rows = 8_388_544
+    assert fa.fa_bwd_workspace_bytes(1, 1, rows, 64) == fa.FA_BWD_NOALLOC_MAX_SCRATCH_BYTES
+    assert fa.fa_bwd_workspace_bytes(1, 1, rows + 1, 64) > fa.FA_BWD_NOALLOC_MAX_SCRATCH_BYTES
+
+    def call(N, B=1, H=1):
+        return fa.fa_bwd_noalloc(A, A, A, A, A, A, A, A, A, B, H, N, 64, 0.125, True, stream=0)
+
+    for B, H, N in ((1, 1, rows), (2, 4, rows // 8)):
+        st = call(N, B, H)
+        assert st != fa.FA_ERR_WORKSPACE and st == fa.FA_ERR_LAUNCH, fa.status_string(st)
+    assert call(rows + 1) == fa.FA_ERR_WORKSPACE
+    assert call(rows // 8 + 1, 2, 4) == fa.FA_ERR_WORKSPACE
+
+
+def test_test_fault_hook_validates_kind(lib):
+    assert fa.fa_test_arm_fault(2) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_test_arm_fault(-1) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_test_arm_fault(0) == fa.FA_OK
