@@ -1,7 +1,8 @@
 """The five workload shapes at full size on the GPU, in the launch
-configuration the benchmark uses, against the fp64 oracle on sampled heads,
-rows and keys; plus properties that hold at any size over whole tensors."""
-import numpy as np
+configuration the benchmark uses, against the fp64 oracle over every element
+of o, lse, dq, dk and dv ("FlashAttention and GPU Memory", chapters 08 and
+12: the tiled result equals the plain definition up to rounding), plus the
+gradient identities that hold at any size."""
 import pytest
 import torch
 
@@ -13,16 +14,10 @@ pytestmark = pytest.mark.gpu
 CASES = [(name, c) for name, w in inputs.WORKLOADS.items() for c in w.causal]
 
 
-def sample_rows(N, rng, n_random=48):
-    fixed = [0, 1, 2, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
-    rows = sorted({r for r in fixed + list(rng.integers(0, N, n_random)) if 0 <= r < N})
-    return rows
-
-
 @pytest.mark.parametrize("name,causal", CASES, ids=[f"{n}-{'causal' if c else 'full'}" for n, c in CASES])
 def test_workload_full_size(name, causal):
     w = inputs.WORKLOADS[name]
-    B, H, N, d, BH = w.B, w.H, w.N, w.d, w.BH
+    BH, N, d = w.BH, w.N, w.d
     scale = w.softmax_scale
     x = inputs.workload_inputs(w)
     g = {k: t.cuda() for k, t in x.items()}
@@ -30,9 +25,6 @@ def test_workload_full_size(name, causal):
     dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["dO"], causal=causal, scale=scale)
     parity.check_status()
 
-    # whole-tensor properties
-    for t in (o, lse, dq, dk, dv):
-        assert torch.isfinite(t.float()).all()
     # Rows of dS sum to zero, so the keys' dk sum to zero in every head; the keys'
     # dv sum to the queries' dO sum (rows of P sum to one). Compared per head
     # against the Frobenius norm of the gradient, which bounds bf16 rounding.
@@ -41,11 +33,10 @@ def test_workload_full_size(name, causal):
     dO_sum = g["dO"].float().reshape(BH, N, d).sum(dim=1)
     dv_ratio = ((dv32.sum(dim=1) - dO_sum).norm(dim=1) / dv32.norm(dim=(1, 2))).max().item()
     assert dk_ratio <= 0.05 and dv_ratio <= 0.05, (dk_ratio, dv_ratio)
+    del g, dk32, dv32, dO_sum
+    torch.cuda.empty_cache()
 
-    rng = np.random.default_rng(w.seed)
-    rows = sample_rows(N, rng)
-    fwd_heads = sorted({0, BH // 2, BH - 1})
-    parity.check_fwd(x, o, lse, scale, causal, rows=rows, heads=fwd_heads)
-    bwd_heads = [BH - 1] if N >= 8192 else sorted({0, BH - 1})
-    keys = sample_rows(N, np.random.default_rng(w.seed + 1))
-    parity.check_bwd(x, dq, dk, dv, scale, causal, heads=bwd_heads, qrows=rows, keys=keys)
+    err = parity.whole_tensor_errors(x, o, lse, dq, dk, dv, scale, causal)
+    err["dk_sum_ratio"], err["dv_sum_ratio"] = dk_ratio, dv_ratio
+    parity.report(f"{name} {'causal' if causal else 'non-causal'} (every element)", err)
+    parity.assert_within_tolerances(err)
