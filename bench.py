@@ -22,6 +22,9 @@ is the HBM bandwidth of its algorithmic bytes.
 ``--dropout P256`` runs the step with dropout of probability P256 / 256
 (fa_fwd_dropout, fa_bwd_dropout; a new Philox mask every step).
 
+``--all-workloads`` (opt-in, one GPU) prints one such line for every workload
+shape and masking in turn.
+
 ``--workload fp8_<B>_<H>_<N>_<causal|noncausal>`` measures the 8-bit forward
 (fa_fwd_fp8, d = 128, E4M3 q, k, v with per-tensor factors): a step is one
 call, and the metric is its matmul TFLOP/s against the 8-bit dense peak.
@@ -269,6 +272,8 @@ def run_gpu(args, w, causal: bool):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = int(stream.cuda_stream)
+    io_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, dO, o, dq, dk, dv))
+    extra_bytes = lse.numel() * lse.element_size() + ws_bytes
 
     p256 = args.dropout  # dropout probability p256 / 256; every step draws a new mask (offset = step)
 
@@ -300,13 +305,25 @@ def run_gpu(args, w, causal: bool):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # A step whose tensors fit in L2 twice over would find the previous step's in
+    # it: such workloads write a 2 x L2 buffer between steps (outside the step's
+    # events) and time the steps by their events alone.
+    step_bytes = 5 * B * H * N * d * 2
+    flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev) if step_bytes < 2 * L2_BYTES else None
     for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
         fwd()
         bwd()
     barrier()
     st = fa.fa_device_status(True)
     if st != fa.FA_OK:
         raise fa.FAError(st, "warm-up")
+    # device memory around the timed region: the library allocates nothing, so
+    # neither torch's peak nor the device's free memory may move
+    free_before, _ = torch.cuda.mem_get_info(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    alloc_before = torch.cuda.memory_allocated(dev)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -324,6 +341,8 @@ def run_gpu(args, w, causal: bool):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for step, (e0, e1, e2) in enumerate(ev):
+        if flush is not None:
+            flush.zero_()  # evicts the previous step's tensors from L2, outside the step's events
         e0.record(stream)
         fwd(step)
         e1.record(stream)
@@ -332,9 +351,18 @@ def run_gpu(args, w, causal: bool):
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
+    memory = {
+        "io_bytes": io_bytes, "extra_bytes": extra_bytes, "extra_bytes_per_row": extra_bytes / (B * H * N),
+        "n_by_n_bf16_bytes": B * H * N * N * 2,
+        "torch_peak_growth_bytes": torch.cuda.max_memory_allocated(dev) - alloc_before,
+        "device_free_delta_bytes": free_before - torch.cuda.mem_get_info(dev)[0],
+        "note": "extra = lse + fa_bwd workspace (D and work counters): linear in N; io = q, k, v, dO, o, dq, dk, dv",
+    }
     elapsed = t_start.elapsed_time(t_end) / 1e3
     fwd_s = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / 1e3 / args.steps
     bwd_s = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / 1e3 / args.steps
+    if flush is not None:
+        elapsed = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / 1e3
     st = fa.fa_device_status(True)
     if st != fa.FA_OK:
         raise fa.FAError(st, "timed region")
@@ -402,7 +430,22 @@ def run_gpu(args, w, causal: bool):
     peaks = measured_peaks()
     burst = peaks["bf16_tflops"]
     sustained = peaks.get("bf16_tflops_sustained", burst)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # A timed region well under a second is a burst: the power cap has no time to
+    # pull the clocks down, so the burst peak is the denominator; a seconds-long
+    # region takes the sustained one.
+    long_region = elapsed >= 1.0
+    peak = sustained if long_region else burst
     achieved = f_bwd / bwd_s / 1e12
+    b_fwd = model.fwd_bytes(B, H, N, d)
+    b_bwd = model.bwd_bytes(B, H, N, d)
+
+    def roof(flops, nbytes, secs):
+        t_tc, t_hbm = flops / (peak * 1e12), nbytes / (hbm * 1e9)
+        return {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_roofline_ms": round(max(t_tc, t_hbm) * 1e3, 4),
+                "frac": round(max(t_tc, t_hbm) / secs, 4)}
+
+    bwd_roof = roof(f_bwd, b_bwd, bwd_s)
     traffic = None if p256 else kernel_traffic("fa_bwd.cu", f"fa_bwd<{d},{str(causal).lower()}>")
     result = {
         "metric": METRIC,
@@ -423,23 +466,34 @@ def run_gpu(args, w, causal: bool):
             "step": "fa_fwd then fa_bwd (O, lse, dq, dk, dv)" if not p256 else
                     f"fa_fwd_dropout then fa_bwd_dropout, p = {p256}/256, Philox4x32-10 mask, a new offset every step",
             "parallelism": f"replicas over (batch, head): {world} x {B * H} heads",
-            "l2": f"inputs larger than L2: {5 * B * H * N * d * 2 / 1e6:.0f} MB of bf16 tensors per step vs "
-                  f"{L2_BYTES / 1e6:.0f} MB L2; no flush",
+            "l2": (f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of bf16 tensors per step vs "
+                   f"{L2_BYTES / 1e6:.0f} MB L2; no flush" if flush is None else
+                   f"{step_bytes / 1e6:.1f} MB of bf16 tensors per step vs {L2_BYTES / 1e6:.0f} MB L2: a "
+                   f"{2 * L2_BYTES / 1e6:.0f} MB buffer is written between steps, and the steps are timed by "
+                   "their own events"),
             "flops_per_step": f_fwd + f_bwd,
         },
         "fwd": {"ms": round(fwd_s * 1e3, 4), "tflops": round(f_fwd / fwd_s / 1e12, 2),
-                "pct_of_peak": round(100 * f_fwd / fwd_s / 1e12 / burst, 2)},
+                "pct_of_peak": round(100 * f_fwd / fwd_s / 1e12 / burst, 2),
+                "gbs": round(b_fwd / fwd_s / 1e9, 1), "roofline": roof(f_fwd, b_fwd, fwd_s)},
         "bwd": {"ms": round(bwd_s * 1e3, 4), "tflops": round(achieved, 2),
-                "pct_of_peak": round(100 * achieved / burst, 2)},
+                "pct_of_peak": round(100 * achieved / burst, 2),
+                "gbs": round(b_bwd / bwd_s / 1e9, 1), "roofline": bwd_roof},
         "pct_of_peak": round(100 * value / 1e12 / world / burst, 2),
         "peak_basis": f"{peaks['source']} dense bf16 burst {burst} TFLOP/s per GPU",
         "roofline": {
             "kernel": "fa_bwd call: D prep + dK/dV kernel + dQ kernel (shares in profiles/)",
-            "bound": "tensor", "achieved": round(achieved, 2), "peak": sustained, "unit": "TFLOP/s",
-            "frac": round(achieved / sustained, 4), "traffic": traffic,
-            "peak_basis": f"{peaks['source']} sustained dense bf16 (kernel timed inside a long step)",
-            "algorithmic_flops_per_launch": f_bwd,
+            "bound": bwd_roof["bound"],
+            "achieved": round(achieved, 2) if bwd_roof["bound"] == "tensor" else round(b_bwd / bwd_s / 1e9, 1),
+            "peak": peak if bwd_roof["bound"] == "tensor" else hbm,
+            "unit": "TFLOP/s" if bwd_roof["bound"] == "tensor" else "GB/s",
+            "frac": bwd_roof["frac"], "traffic": traffic,
+            "peak_basis": (f"{peaks['source']} {'sustained' if long_region else 'burst'} dense bf16: the timed "
+                           f"region lasts {elapsed:.3f} s" if bwd_roof["bound"] == "tensor" else
+                           f"{peaks['source']} HBM copy bandwidth"),
+            "algorithmic_flops_per_launch": f_bwd, "algorithmic_bytes_per_launch": b_bwd,
         },
+        "memory": memory,
         "e2e": {"value": round(e2e_value / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "schedule": "copy-in, compute and copy-out on three streams, two buffer sets: neighbouring steps overlap"},
@@ -453,6 +507,7 @@ def run_gpu(args, w, causal: bool):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+    return result
 
 
 # ---------------------------------------------------------------------- decoding forward
@@ -782,9 +837,19 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=120.0, help="seconds for --impl reference")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="one line per workload shape and masking (opt-in; one GPU): the same step and keys")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.all_workloads:
+        if dist_env()[1] != 1 or args.impl != "ours":
+            raise SystemExit("--all-workloads runs on one GPU, our implementation only")
+        for name, wl in inputs.WORKLOADS.items():
+            for causal in wl.causal:
+                args.workload = f"{name}_{'causal' if causal else 'noncausal'}"
+                run_gpu(args, wl, causal)
+        return
     c = fp8_spec(args.workload)
     if c is not None:
         if args.impl == "reference":
