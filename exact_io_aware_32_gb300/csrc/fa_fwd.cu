@@ -389,13 +389,20 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // Row maximum over eight independent chains of 16 scores (chain i takes
+      // columns 2 i, 2 i + 1 of every 16-column group), then a tree: the
+      // dependent chain is 8 + 2 instructions deep instead of 32.
+      float mxc[8];
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        mx0 = fmax3(mx0, __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[c >> 5][(c & 31) + 2]), __uint_as_float(sr[c >> 5][(c & 31) + 3]));
-      }
-      const float mx = fmaxf(mx0, mx1);
+      for (int i = 0; i < 8; ++i)
+        mxc[i] = fmaxf(__uint_as_float(sr[0][2 * i]), __uint_as_float(sr[0][2 * i + 1]));
+#pragma unroll
+      for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          mxc[i] = fmax3(mxc[i], __uint_as_float(sr[c >> 5][(c & 31) + 2 * i]),
+                         __uint_as_float(sr[c >> 5][(c & 31) + 2 * i + 1]));
+      const float mx = fmax3(fmax3(mxc[0], mxc[1], mxc[2]), fmax3(mxc[3], mxc[4], mxc[5]), fmaxf(mxc[6], mxc[7]));
       float alpha = 1.f;
       bool move;
       if constexpr (FP8) {
@@ -416,7 +423,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
         }
       }
       const bool rescale = __any_sync(0xffffffffu, move && j > 0);
-      float2 sum = make_float2(0.f, 0.f);
+      // four partial row sums, so that the additions do not form one long chain
+      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // a row that has seen no key yet (possible within a key range) keeps m_ref = -inf and P = 0
       const float m_use = (m_ref == -INFINITY ? 0.f : m_ref) - (FP8 ? kP8Bias : 0.f);
       const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_use, -m_use);
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
             const float2 x1 =
                 ffma2(make_float2(__uint_as_float(sr[ch][cc + 2]), __uint_as_float(sr[ch][cc + 3])), scale2, shift2);
             const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
-            sum = fadd2(sum, fadd2(p0, p1));
+            sum4[(c >> 2) & 3] = fadd2(sum4[(c >> 2) & 3], fadd2(p0, p1));
             pk[c >> 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
           }
           tmem_st16(t_s + 16 * half, pk);
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
             const float2 x =
                 ffma2(make_float2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), scale2, shift2);
             const float2 p = make_float2(ex2(x.x), ex2(x.y));
-            sum = fadd2(sum, p);
+            sum4[(c >> 1) & 3] = fadd2(sum4[(c >> 1) & 3], p);
             pk[c >> 1] = pack_bf16x2(p.x, p.y);
           }
           if constexpr (DROP) {
@@ -475,6 +483,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
           tmem_st16(t_s + 16 * ch, pk);
         }
       }
+      const float2 sum = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
       l_sum = l_sum * alpha + (sum.x + sum.y);
       if (rescale) {
 #pragma unroll 1
