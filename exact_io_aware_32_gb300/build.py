@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfa.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_noalloc.cu", "schedule.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_persist.cu", "fa_bwd.cu", "fa_bwd_noalloc.cu", "schedule.cu"]
 HEADERS = ["ptx.cuh", "block_order.cuh", "fa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

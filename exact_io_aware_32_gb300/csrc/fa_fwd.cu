@@ -637,6 +637,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& args, int num_sms, cudaStream_t stream) {
+  if (fwd_persist_applies(args)) return launch_fwd_persist(args, num_sms, stream);
   FwdArgs a = args;
   // a CTA's fixed cost (loads before the first product, epilogue) is about two key blocks of work
   const int rows = fwd_rows_per_cta(a.d), slots = num_sms * fwd_ctas_per_sm(a.d);

@@ -113,5 +113,9 @@ cudaError_t launch_fwd(const FwdArgs& a, int num_sms, cudaStream_t stream);
 constexpr int kMaxKeySplits = 32;
 int pick_key_splits(int BH, int Nq, int Nk, int num_slots, int rows_per_cta);
 cudaError_t launch_bwd(const BwdArgs& a, int num_sms, cudaStream_t stream);
+// The persistent d = 64 forward (fa_fwd_persist.cu): whether it takes these
+// arguments (d = 64, 16-bit, no padding masks, key ranges or dropout), and its launch.
+bool fwd_persist_applies(const FwdArgs& a);
+cudaError_t launch_fwd_persist(const FwdArgs& a, int num_sms, cudaStream_t stream);
 
 }  // namespace fa
