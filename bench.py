@@ -446,7 +446,7 @@ def run_gpu(args, w, causal: bool):
                 "frac": round(max(t_tc, t_hbm) / secs, 4)}
 
     bwd_roof = roof(f_bwd, b_bwd, bwd_s)
-    traffic = None if p256 else kernel_traffic("fa_bwd.cu", f"fa_bwd<{d},{str(causal).lower()}>")
+    traffic = None if p256 else kernel_traffic("fa_bwd.cu", f"bwd:{args.workload}")
     result = {
         "metric": METRIC,
         "value": round(value / 1e12, 2),
