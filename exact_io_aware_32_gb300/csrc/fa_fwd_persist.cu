@@ -14,8 +14,10 @@
 // each CTA (two per SM) runs a sequence of tiles instead, so that they overlap
 // the neighbouring tiles' work:
 //   - Q has two slots: the next tile's Q is loaded while the current tile runs;
-//   - O has two TMEM buffers: the next tile's first products run while the
-//     softmax warpgroup reads out and stores the previous tile's O;
+//   - P has TMEM columns of its own, apart from S: once the softmax has read S
+//     of a block into registers, S of the next block (of this tile or the next)
+//     is computed while the softmax works, so the softmax warps never wait for
+//     two products in a row;
 //   - the K/V rings, their barriers and the S/P barriers count key blocks over
 //     the CTA's whole run, so the pipeline never drains between tiles.
 // Tiles are dealt to CTAs statically, in rounds of one tile per CTA, every
@@ -53,8 +55,9 @@ struct PCfg {
   // that dynamic shared memory starts on a 1024-byte boundary.
   static constexpr int kSmemBytes = kOffBar + 256;
   static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit an SM's shared memory");
-  static constexpr uint32_t kColS = 0;    // S fp32 (P as bf16 over its first 64 columns)
-  static constexpr uint32_t kColO = 128;  // O buffers: [128, 192) and [192, 256)
+  static constexpr uint32_t kColS = 0;    // S fp32, 128 columns
+  static constexpr uint32_t kColP = 128;  // P as bf16 pairs, 64 columns
+  static constexpr uint32_t kColO = 192;  // O fp32, 64 columns
   static constexpr uint32_t kTmemCols = 256;
   static constexpr int kThreads = 192;
   static constexpr int kWarpTma = 4, kWarpMma = 5;
@@ -63,8 +66,7 @@ struct PCfg {
 struct PBars {
   uint64_t q_full[2], q_free[2];
   uint64_t k_full[2], k_empty[2], v_full[3], v_empty[3];
-  uint64_t s_full, p_full;
-  uint64_t o_done[2], o_free[2];
+  uint64_t s_full, s_free, p_full, pv_done, o_free;
   uint64_t teardown;
   uint32_t tmem_base;
   int abort;
@@ -112,8 +114,6 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_free[s], 1);
-      mbar_init(&bars.o_done[s], 1);
-      mbar_init(&bars.o_free[s], 128);
     }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
@@ -124,7 +124,10 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
       mbar_init(&bars.v_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, 128);
     mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.o_free, 128);
     mbar_init(&bars.teardown, 1);
     fence_mbar_init();
   }
@@ -192,10 +195,11 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
       mbar_wait_drain(&bars.v_full[x % C::kVStages], (x / C::kVStages) & 1);
   } else if (warp == C::kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per key block: O_t += P V, then S of the next block (which may be the next
-    // tile's first). S overwrites the columns P occupies; the products of one
-    // thread execute in issue order, so PV has read P by then, and when S
-    // completes so has PV (the softmax may then rescale O).
+    // Per key block g: S of block g + 1 as soon as the softmax has read S of
+    // block g (and, for a tile's first block, its Q has landed), then O += P V
+    // once P of block g is written. At a tile's last block P V goes first, so
+    // that the epilogue can read O out sooner, and S of the next tile's first
+    // block follows.
     constexpr uint32_t kIdS = idesc_bf16(128, C::BN, false, false);  // Q, K both K-major
     constexpr uint32_t kIdO = idesc_bf16(128, C::D, false, true);    // P from TMEM, V MN-major
     const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
@@ -210,39 +214,51 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
       mma_commit(&bars.s_full);
       mma_commit(&bars.k_empty[g % C::kKStages]);  // S is K's only reader
     };
-    bool ok = true;
-    int g = 0;
-    for (int i = 0; ok; ++i) {
-      const PTile t = ptile<CAUSAL>(a, i, nqblk);
-      if (t.nb == 0) break;
-      const int slot = i & 1;
-      const uint32_t d_o = tmem + C::kColO + slot * C::D;
-      ok = warp_wait2(&bars.q_full[slot], (i >> 1) & 1, &bars.k_full[g % C::kKStages], (g / C::kKStages) & 1,
-                      abort_flag);
-      if (!ok) break;
+    // S of block g + 1 (Q slot 'slot'); 'new_tile' adds the wait for that tile's Q
+    auto next_s = [&](int g, int slot, bool new_tile, int i_next) -> bool {
+      const int ks = (g + 1) % C::kKStages;
+      bool w = warp_wait2(&bars.s_free, g & 1, &bars.k_full[ks], ((g + 1) / C::kKStages) & 1, abort_flag);
+      if (w && new_tile) w = warp_wait(&bars.q_full[slot], (i_next >> 1) & 1, abort_flag);
+      if (!w) return false;
       tc_fence_after();
-      if (elect_one()) issue_s(slot, g);
+      if (elect_one()) issue_s(slot, g + 1);
       __syncwarp();
-      // O buffer 'slot' was last read out by the epilogue of tile i - 2
-      if (!(ok = warp_wait(&bars.o_free[slot], ((i >> 1) & 1) ^ 1, abort_flag))) break;
+      return true;
+    };
+    bool ok = warp_wait2(&bars.q_full[0], 0, &bars.k_full[0], 0, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) issue_s(0, 0);
+      __syncwarp();
+    }
+    const uint32_t d_o = tmem + C::kColO;
+    int g = 0;
+    PTile t = ptile<CAUSAL>(a, 0, nqblk);
+    for (int i = 0; ok && t.nb > 0; ++i) {
+      const int slot = i & 1;
+      const PTile tn = ptile<CAUSAL>(a, i + 1, nqblk);
       for (int j = 0; j < t.nb; ++j, ++g) {
+        const bool last = j + 1 == t.nb;
+        if (!last && !(ok = next_s(g, slot, false, 0))) break;
         const int vs = g % C::kVStages;
-        ok = warp_wait2(&bars.v_full[vs], (g / C::kVStages) & 1, &bars.p_full, g & 1, abort_flag);
-        if (ok && j + 1 < t.nb) ok = warp_wait(&bars.k_full[(g + 1) % C::kKStages], ((g + 1) / C::kKStages) & 1, abort_flag);
+        ok = warp_wait2(&bars.p_full, g & 1, &bars.v_full[vs], (g / C::kVStages) & 1, abort_flag);
+        // the first P V of a tile overwrites O: the previous tile's epilogue has read it out
+        if (ok && j == 0 && i > 0) ok = warp_wait(&bars.o_free, (i - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t vo = (uint32_t)(vs * C::kTileBytes) >> 4;
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk)  // P columns [8 kk, 8 kk + 8), V rows [16 kk, 16 kk + 16)
-            mma_ts(d_o, tmem + C::kColS + kk * 8, dv0 + vo + kk * ((16 * 128) >> 4), kIdO,
+            mma_ts(d_o, tmem + C::kColP + kk * 8, dv0 + vo + kk * ((16 * 128) >> 4), kIdO,
                    (j > 0 || kk > 0) ? 1u : 0u);
-          if (j == t.nb - 1) mma_commit(&bars.o_done[slot]);
+          mma_commit(&bars.pv_done);
           mma_commit(&bars.v_empty[vs]);
-          if (j + 1 < t.nb) issue_s(slot, g + 1);
         }
         __syncwarp();
+        if (last && tn.nb > 0 && !(ok = next_s(g, slot ^ 1, true, i + 1))) break;
       }
+      t = tn;
     }
     if (elect_one()) mma_commit(&bars.teardown);
     __syncwarp();
@@ -252,6 +268,8 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
     const int r = warp * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS;
+    const uint32_t t_p = tmem + lane_off + C::kColP;
+    const uint32_t t_o = tmem + lane_off + C::kColO;
     const float sl2 = a.scale_log2;
     const int off = a.Nk - a.Nq;
     bool ok = true;
@@ -261,7 +279,6 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
       if (t.nb == 0) break;
       const int slot = i & 1;
       const int r0 = t.qblk * 128, row = r0 + r;
-      const uint32_t t_o = tmem + lane_off + C::kColO + slot * C::D;
       float m_ref = -INFINITY;  // exponent reference, log2 units of scaled scores
       float l_sum = 0.f;        // sum of 2^(s * sl2 - m_ref) over the keys seen so far
       for (int j = 0; j < t.nb; ++j, ++g) {
@@ -273,6 +290,8 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
         for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
         // only blocks that reach past the tile's first row's last key, or past
         // the last key, need masking: a hidden score becomes -inf, so P = 0
         const int kv0 = j * C::BN;
@@ -304,20 +323,39 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
         float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
         const float2 scale2 = make_float2(sl2, sl2), shift2 = make_float2(-m_ref, -m_ref);
-        // P as bf16 pairs over the first 64 columns of S, 32 scores at a time
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
+        // P as bf16 pairs, 32 scores at a time. P and O of the previous block are free
+        // once its P V has completed (a tile's first block: the previous tile's
+        // epilogue waited for that already); the first two chunks are computed before
+        // that wait, packed in place (pair c / 2 of a chunk into word c / 2, already read).
+        auto chunk = [&](int ch) {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 x =
                 ffma2(make_float2(__uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1])), scale2, shift2);
             const float2 p = make_float2(ex2(x.x), ex2(x.y));
             sum4[(c >> 1) & 3] = fadd2(sum4[(c >> 1) & 3], p);
-            pk[c >> 1] = pack_bf16x2(p.x, p.y);
+            sr[ch][c >> 1] = pack_bf16x2(p.x, p.y);
           }
-          tmem_st16(t_s + 16 * ch, pk);
+        };
+        auto store = [&](int ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) pk[q] = sr[ch][q];
+          tmem_st16(t_p + 16 * ch, pk);
+        };
+        chunk(0);
+        chunk(1);
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done, (g - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
         }
+        store(0);
+        store(1);
+        chunk(2);
+        store(2);
+        chunk(3);
+        store(3);
         const float2 sum = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
         l_sum = l_sum * alpha + (sum.x + sum.y);
         if (rescale) {
@@ -336,7 +374,7 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
         mbar_arrive(&bars.p_full);
       }
       // Epilogue of tile i; every thread of the warpgroup runs it (named barriers).
-      if (ok) ok = mbar_wait(&bars.o_done[slot], (i >> 1) & 1, abort_flag);
+      if (ok) ok = mbar_wait(&bars.pv_done, (g - 1) & 1, abort_flag);  // the tile's last P V
       ok = __all_sync(0xffffffffu, ok);
       uint8_t* stage = smem + C::kOffQ + slot * C::kTileBytes;  // this tile's Q: its last S has completed
       if (ok) {
@@ -347,7 +385,7 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
         tmem_ld_wait(o[0]);
         tmem_ld_wait(o[1]);
         tc_fence_before();
-        mbar_arrive(&bars.o_free[slot]);  // O is in registers: tile i + 2 may accumulate there
+        mbar_arrive(&bars.o_free);  // O is in registers: tile i + 1 may accumulate there
         const float inv_l = 1.f / l_sum;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
