@@ -373,14 +373,18 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
         break;
       }
       tc_fence_after();
+      // S_t, with the maximum of each 32 columns from the load itself
       uint32_t sr[4][32];
+      float cmax[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32_max(t_s + c * 32, sr[c], cmax[c]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c], cmax[c]);
+      float mx = fmax3(fmax3(cmax[0], cmax[1], cmax[2]), cmax[3], -INFINITY);
       // Only blocks that reach past the tile's first row's last key (the
       // diagonal under the causal mask, one or two blocks) or past key sk - 1 need
-      // masking: there a hidden score becomes -inf, so P = 0 (scale > 0).
+      // masking: there a hidden score becomes -inf, so P = 0 (scale > 0), and the
+      // row maximum is taken again over the scores that stay.
       const int kv0 = (jb + j) * C::BN;
       const bool need_mask = (CAUSAL && kv0 + C::BN - 1 > r0 + off) || kv0 + C::BN > sk;
       if (need_mask) {
@@ -388,21 +392,21 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, FwdCfg<D, FP8>::kCta
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-      }
-      // Row maximum over eight independent chains of 16 scores (chain i takes
-      // columns 2 i, 2 i + 1 of every 16-column group), then a tree: the
-      // dependent chain is 8 + 2 instructions deep instead of 32.
-      float mxc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        mxc[i] = fmaxf(__uint_as_float(sr[0][2 * i]), __uint_as_float(sr[0][2 * i + 1]));
-#pragma unroll
-      for (int c = 16; c < 128; c += 16)
+        // Row maximum over eight independent chains of 16 scores (chain i takes
+        // columns 2 i, 2 i + 1 of every 16-column group), then a tree: the
+        // dependent chain is 8 + 2 instructions deep instead of 32.
+        float mxc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          mxc[i] = fmax3(mxc[i], __uint_as_float(sr[c >> 5][(c & 31) + 2 * i]),
-                         __uint_as_float(sr[c >> 5][(c & 31) + 2 * i + 1]));
-      const float mx = fmax3(fmax3(mxc[0], mxc[1], mxc[2]), fmax3(mxc[3], mxc[4], mxc[5]), fmaxf(mxc[6], mxc[7]));
+          mxc[i] = fmaxf(__uint_as_float(sr[0][2 * i]), __uint_as_float(sr[0][2 * i + 1]));
+#pragma unroll
+        for (int c = 16; c < 128; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mxc[i] = fmax3(mxc[i], __uint_as_float(sr[c >> 5][(c & 31) + 2 * i]),
+                           __uint_as_float(sr[c >> 5][(c & 31) + 2 * i + 1]));
+        mx = fmax3(fmax3(mxc[0], mxc[1], mxc[2]), fmax3(mxc[3], mxc[4], mxc[5]), fmaxf(mxc[6], mxc[7]));
+      }
       float alpha = 1.f;
       bool move;
       if constexpr (FP8) {

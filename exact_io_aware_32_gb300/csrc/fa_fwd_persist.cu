@@ -285,33 +285,38 @@ __global__ void __launch_bounds__(PCfg::kThreads, 2) fa_fwd_persist_kernel(const
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, g & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
+        // S, with the maximum of each 32 columns from the load itself
         uint32_t sr[4][32];
+        float cmax[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_max(t_s + c * 32, sr[c], cmax[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c], cmax[c]);
         tc_fence_before();
         mbar_arrive(&bars.s_free);  // S is in registers: the next block's S may overwrite it
+        float mx = fmax3(fmax3(cmax[0], cmax[1], cmax[2]), cmax[3], -INFINITY);
         // only blocks that reach past the tile's first row's last key, or past
-        // the last key, need masking: a hidden score becomes -inf, so P = 0
+        // the last key, need masking: a hidden score becomes -inf, so P = 0, and
+        // the row maximum is taken again over the scores that stay
         const int kv0 = j * C::BN;
         if ((CAUSAL && kv0 + C::BN - 1 > r0 + off) || kv0 + C::BN > a.Nk) {
           const int lim = (CAUSAL ? min(row + off, a.Nk - 1) : a.Nk - 1) - kv0;  // keep column c iff c <= lim
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-        }
-        // row maximum over eight chains of 16 scores, then a tree
-        float mxc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mxc[q] = fmaxf(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
-#pragma unroll
-        for (int c = 16; c < 128; c += 16)
+          // row maximum over eight chains of 16 scores, then a tree
+          float mxc[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            mxc[q] = fmax3(mxc[q], __uint_as_float(sr[c >> 5][(c & 31) + 2 * q]),
-                           __uint_as_float(sr[c >> 5][(c & 31) + 2 * q + 1]));
-        const float mx = fmax3(fmax3(mxc[0], mxc[1], mxc[2]), fmax3(mxc[3], mxc[4], mxc[5]), fmaxf(mxc[6], mxc[7]));
+            mxc[q] = fmaxf(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
+#pragma unroll
+          for (int c = 16; c < 128; c += 16)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              mxc[q] = fmax3(mxc[q], __uint_as_float(sr[c >> 5][(c & 31) + 2 * q]),
+                             __uint_as_float(sr[c >> 5][(c & 31) + 2 * q + 1]));
+          mx = fmax3(fmax3(mxc[0], mxc[1], mxc[2]), fmax3(mxc[3], mxc[4], mxc[5]), fmaxf(mxc[6], mxc[7]));
+        }
         float alpha = 1.f;
         const float m_new = fmaxf(m_ref, mx * sl2);
         const bool move = m_new > m_ref + kRescaleThreshold;
