@@ -437,8 +437,12 @@ cudaError_t launch_fwd_persist(const FwdArgs& args, int num_sms, cudaStream_t st
   const int nqblk = (a.Nq + 127) / 128;
   const long long tiles = (long long)a.BH * nqblk;
   const int ctas = (int)std::min<long long>(tiles, 2ll * num_sms);
-  // about one round of tiles per head group, so that the CTAs of a round share K and V in L2
-  a.head_group = std::max(1, std::min(a.BH, ctas / nqblk));
+  // About one round of tiles per head group, so that the CTAs of a round share K
+  // and V in L2. When the K and V of every head fit in L2 together (64 MB here,
+  // half of it), one group instead: the heaviest tiles of all heads go first, and
+  // with few rounds the rounds balance better (the last one is the lightest).
+  const double kv_bytes = 2.0 * 2.0 * (double)a.BH * (double)a.Nk * (double)a.d;
+  a.head_group = kv_bytes <= 64.0e6 ? a.BH : std::max(1, std::min(a.BH, ctas / nqblk));
   auto kern = a.causal ? fa_fwd_persist_kernel<true> : fa_fwd_persist_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
