@@ -159,7 +159,7 @@ constexpr double kLog2e = 1.4426950408889634074;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// The backward of every entry point: arguments validated, then D prep, dK/dV and dQ.
+// The backward of every entry point: arguments validated, then the kernels (launch_bwd).
 int bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
                void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                const int* seqlens_q, const int* seqlens_k, int p256, unsigned long long seed, unsigned int offset,
@@ -184,6 +184,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* o, const
   a.work = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + (need - 256));
   if (!encode_3d(&a.tm_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
       !encode_3d(&a.tm_do, dO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
+      !encode_3d(&a.tm_o, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||
       !encode_3d(&a.tm_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
       !encode_3d(&a.tm_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nk, d, 64, 128) ||
       !encode_3d(&a.tm_dq, dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, Nq, d, 64, 128) ||

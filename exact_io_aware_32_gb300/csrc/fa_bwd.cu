@@ -15,6 +15,10 @@
 //      accumulates dK and dV in tensor memory (TMEM).
 //   3. bwd_dq:   one CTA per 128-row query block, looping over 128-key blocks;
 //      accumulates dQ in TMEM.
+// At d = 64 the dQ kernel runs first and forms D itself, from the dO tile it
+// loads anyway and an O tile loaded beside it, and writes it for the dK/dV
+// kernel after it: a small start kernel only resets the work counters, and dO
+// is read from device memory twice instead of three times.
 // Both main kernels rebuild S and dP; dQ is summed on chip in a fixed order,
 // so the result is deterministic and no fp32 atomics are needed (on GB300 the
 // L2's atomic-add rate, about 1.1-1.4e12 fp32 adds/s, would otherwise bound
@@ -757,9 +761,13 @@ struct DqCfg {
   static constexpr int kKStages = D == 128 ? 3 : 4;
   static constexpr int kVStages = D == 128 ? 2 : 3;
   static constexpr int kItemSlots = 4;  // tiles fetched ahead by the producer
+  // D = 64: an O tile beside dO, from which the warpgroups form D for the tile
+  static constexpr bool kFuseD = D == 64;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTileBytes;
-  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffO = 2 * kTileBytes;  // (kFuseD only)
+  static constexpr int kOffK = (kFuseD ? 3 : 2) * kTileBytes;
+  static_assert(!kFuseD || kOffO + kTileBytes <= kOffK, "the O tile overlaps the K ring");
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
@@ -773,7 +781,7 @@ struct DqCfg {
 struct DqBarriers {
   uint64_t item_full[4], item_empty[4];  // tile ring: producer -> MMA warp and warpgroups
   uint64_t q_full, qt_ready;             // Q buffer (one tile) loaded; Q copied into TMEM
-  uint64_t do_full, do_empty;            // dO buffer (one tile)
+  uint64_t do_full, do_empty;            // dO buffer (one tile; with kFuseD also the O buffer)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, dp_free, ds_ready, dq_tile, teardown, teardown_q;
   uint64_t ep_staged, dq_stored;        // dQ of a tile staged in the Q buffer; its store has read it
@@ -847,7 +855,8 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.qt_ready, 256);
     mbar_init(&bars.do_full, 1);
-    mbar_init(&bars.do_empty, 1);
+    // the tile's last dP; with kFuseD also every warpgroup thread, once it has formed D
+    mbar_init(&bars.do_empty, C::kFuseD ? 1 + 256 : 1);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -970,10 +979,12 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
         if (j == 0) {
           if (!(ok = warp_wait(&bars.do_empty, (k & 1) ^ 1, abort_flag))) break;
           if (elect_one()) {
-            mbar_arrive_expect_tx(&bars.do_full, C::kTileBytes);
+            mbar_arrive_expect_tx(&bars.do_full, (C::kFuseD ? 2 : 1) * C::kTileBytes);
             for (int pn = 0; pn < D / 64; ++pn)
               tma_load_3d(smem + C::kOffDO + pn * kPanelBytes, &a.tm_do, &bars.do_full, pn * 64, t.qblk * C::BQ,
                           t.bh);
+            if constexpr (C::kFuseD)
+              tma_load_3d(smem + C::kOffO, &a.tm_o, &bars.do_full, 0, t.qblk * C::BQ, t.bh);
           }
           __syncwarp();
           do_loads = k + 1;
@@ -1127,7 +1138,7 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     auto load_row_terms = [&](const DqTile& t, float& lse_raw, float& d_raw) {
       const int q = min(t.qblk * C::BQ + r, Nq - 1);
       lse_raw = a.lse[(size_t)t.bh * Nq + q];
-      d_raw = a.Dsum[(size_t)t.bh * Nq + q];
+      d_raw = C::kFuseD ? 0.f : a.Dsum[(size_t)t.bh * Nq + q];  // (formed in the tile's first block)
     };
     auto row_terms = [&](const DqTile& t, float lse_raw, float d_raw, float& lse2, float& dsum) {
       const bool in = t.qblk * C::BQ + r < (VARLEN ? t.sq : Nq);
@@ -1161,6 +1172,30 @@ __global__ void __launch_bounds__(352, 1) fa_bwd_dq_kernel(const __grid_constant
     }
     while (ok) {
       const int q = t.qblk * C::BQ + r;
+      if constexpr (C::kFuseD) {
+        // D of this thread's row, dO . O over the row's 64 features (every
+        // warpgroup thread forms its row's D; warpgroup 0 also writes it for the
+        // dK/dV kernel), then the dO and O tiles are released to the producer
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_full, k & 1, abort_flag));
+        if (!ok) break;
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int off = r * 128 + ((c ^ (r & 7)) << 4);  // 16-byte chunk c of the 128-byte-swizzled row
+          const uint4 x = *reinterpret_cast<const uint4*>(smem + C::kOffDO + off);
+          const uint4 y = *reinterpret_cast<const uint4*>(smem + C::kOffO + off);
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc0 = fmaf(__uint_as_float(xs[i] << 16), __uint_as_float(ys[i] << 16), acc0);
+            acc1 = fmaf(__uint_as_float(xs[i] & 0xFFFF0000u), __uint_as_float(ys[i] & 0xFFFF0000u), acc1);
+          }
+        }
+        mbar_arrive(&bars.do_empty);
+        const float drow = acc0 + acc1;
+        if (w == 0 && q < Nq) a.Dsum[(size_t)t.bh * Nq + q] = drow;
+        dsum = q < (VARLEN ? t.sq : Nq) ? drow : 0.f;
+      }
       for (int j = 0; j < t.nk; ++j) {
         const int gj = g + j;
         ok = mbar_wait(&bars.s_full, gj & 1, abort_flag);
@@ -1344,29 +1379,51 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __grid_constant_
   }
 }
 
+// The d = 64 backward's first kernel (its dQ kernel forms D): the work counters
+// of the two main kernels are reset, and one thread per sequence checks its lengths.
+__global__ void __launch_bounds__(32) fa_bwd_start_kernel(const __grid_constant__ BwdArgs a) {
+  if (threadIdx.x < 2) a.work[threadIdx.x] = 0u;
+  if (a.seqlens_q || a.seqlens_k)
+    for (int b = (int)threadIdx.x; b < a.BH / a.H; b += 32) {
+      int sq, sk;
+      if (seq_lens(a.seqlens_q, a.seqlens_k, b, a.Nq, a.Nk, a.causal != 0, sq, sk)) atomicOr(a.status, kStatusBadLength);
+    }
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const BwdArgs& a, int num_sms, cudaStream_t stream) {
-  const long long rows = (long long)a.BH * a.Nq;
-  const int rows_per_block = 256 / (D / 8);
-  fa_bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   const bool varlen = a.seqlens_q || a.seqlens_k;
   auto kv = varlen ? fa_bwd_dkdv_kernel<D, CAUSAL, true> : fa_bwd_dkdv_kernel<D, CAUSAL, false>;
   if (a.drop_p256 > 0) kv = fa_bwd_dkdv_kernel<D, CAUSAL, false, true>;  // dropout: no lengths
+  auto kq = varlen ? fa_bwd_dq_kernel<D, CAUSAL, true> : fa_bwd_dq_kernel<D, CAUSAL, false>;
+  if (a.drop_p256 > 0) kq = fa_bwd_dq_kernel<D, CAUSAL, false, true>;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kSmemBytes)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
       cudaSuccess)
     return e;
   // persistent: one CTA per SM at most (both main kernels take their tiles from counters)
   const long long kv_tiles = (long long)a.BH * ((a.Nk + 127) / 128), q_tiles = (long long)a.BH * ((a.Nq + 127) / 128);
-  kv<<<(unsigned)std::min<long long>(kv_tiles, num_sms), 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  auto kq = varlen ? fa_bwd_dq_kernel<D, CAUSAL, true> : fa_bwd_dq_kernel<D, CAUSAL, false>;
-  if (a.drop_p256 > 0) kq = fa_bwd_dq_kernel<D, CAUSAL, false, true>;
-  if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kSmemBytes)) !=
-      cudaSuccess)
-    return e;
-  kq<<<(unsigned)std::min<long long>(q_tiles, num_sms), 352, DqCfg<D>::kSmemBytes, stream>>>(a);
+  const unsigned kv_ctas = (unsigned)std::min<long long>(kv_tiles, num_sms);
+  const unsigned q_ctas = (unsigned)std::min<long long>(q_tiles, num_sms);
+  if constexpr (DqCfg<D>::kFuseD) {
+    // the dQ kernel forms D and writes it; the dK/dV kernel reads it after
+    fa_bwd_start_kernel<<<1, 32, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kq<<<q_ctas, 352, DqCfg<D>::kSmemBytes, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kv<<<kv_ctas, 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
+  } else {
+    const long long rows = (long long)a.BH * a.Nq;
+    const int rows_per_block = 256 / (D / 8);
+    fa_bwd_prep_kernel<D><<<(unsigned)((rows + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kv<<<kv_ctas, 352, DkdvCfg<D>::kSmemBytes, stream>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kq<<<q_ctas, 352, DqCfg<D>::kSmemBytes, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

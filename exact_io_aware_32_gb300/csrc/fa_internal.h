@@ -45,6 +45,7 @@ struct FwdArgs {
 struct BwdArgs {
   // bf16, box 64 x 128 x 1, 128B swizzle: q, dO, dq over [BH][Nq][d]; k, v, dk, dv over [BH][Nk][d]
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // loads
+  CUtensorMap tm_o;                     // o, loaded by the d = 64 dQ kernel, which forms D itself
   CUtensorMap tm_dq, tm_dk, tm_dv;      // stores
   const void* o;                        // bf16 [BH][Nq][d]
   const void* dO;                       // bf16 [BH][Nq][d]
