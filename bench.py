@@ -482,7 +482,8 @@ def run_gpu(args, w, causal: bool):
         "pct_of_peak": round(100 * value / 1e12 / world / burst, 2),
         "peak_basis": f"{peaks['source']} dense bf16 burst {burst} TFLOP/s per GPU",
         "roofline": {
-            "kernel": "fa_bwd call: D prep + dK/dV kernel + dQ kernel (shares in profiles/)",
+            "kernel": ("fa_bwd call: D prep + dK/dV kernel + dQ kernel (shares in profiles/)" if d == 128 else
+                       "fa_bwd call: start kernel + dQ kernel (forms D) + dK/dV kernel (shares in profiles/)"),
             "bound": bwd_roof["bound"],
             "achieved": round(achieved, 2) if bwd_roof["bound"] == "tensor" else round(b_bwd / bwd_s / 1e9, 1),
             "peak": peak if bwd_roof["bound"] == "tensor" else hbm,
