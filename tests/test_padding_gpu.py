@@ -109,11 +109,14 @@ def test_full_lengths_are_no_mask(causal):
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-def test_out_of_range_lengths_are_clamped_and_reported():
+@pytest.mark.parametrize("d", [64, 128])
+def test_out_of_range_lengths_are_clamped_and_reported(d):
     """A length outside [1, N] (or, under the causal mask, a query length above
     the key length) is clamped on the device and reported by fa_device_status
-    as an invalid argument; the results are those of the clamped lengths."""
-    B, H, Nq, Nk, d = 3, 2, 150, 400, 64
+    as an invalid argument; the results are those of the clamped lengths. (The
+    backward checks the lengths in its first kernel: the D prep at d = 128, the
+    start kernel at d = 64.)"""
+    B, H, Nq, Nk = 3, 2, 150, 400
     _, g = kv_inputs(B, H, Nq, Nk, d, seed=91)
     bad_q, bad_k = lens_gpu([0, 999, 200]), lens_gpu([400, 5000, 100])
     good_q, good_k = lens_gpu([1, 150, 100]), lens_gpu([400, 400, 100])  # causal: row length 150 cut to 100
