@@ -65,7 +65,7 @@ struct PCfg {
 
 struct PBars {
   uint64_t q_full[2], q_free[2];
-  uint64_t k_full[PCfg::kKStages], k_empty[PCfg::kKStages], v_full[PCfg::kVStages], v_empty[PCfg::kVStages];
+  uint64_t k_full[2], k_empty[2], v_full[3], v_empty[3];
   uint64_t s_full, s_free, p_full, pv_done, o_free;
   uint64_t teardown;
   uint32_t tmem_base;
